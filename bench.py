@@ -1,0 +1,439 @@
+"""Benchmark of the FP8 hot path on one GB300 (replicas across GPUs).
+
+One step = one pass over every step of the path on synthetic inputs already
+resident in HBM:
+  * per-tensor current scaling linear forward (X 256x1024 with +-30 outliers,
+    W 1024x1024): amax, compute_scale, cast, GEMM with fp32 output;
+  * 13B-class FFN layer forward + backward with per-tensor delayed scaling
+    (history 1024): X 16384x5120, W 20480x5120 (E4M3), dY 16384x20480 (E5M2),
+    each cast row- and column-wise with fused amax; fprop, dgrad, wgrad GEMMs;
+    three history updates;
+  * MXFP8 forward (1x32 blocks, E8M0): X 16384x8192, W 28672x8192 cast row- and
+    column-wise; block-scaled GEMM M=16384 N=28672 K=8192, bf16 output;
+  * per-block forward (1x128 activations, 128x128 weights, fp32 scales), Llama-2-7B
+    MLP up-projection: X 8192x4096, W 11008x4096; GEMM M=8192 N=11008 K=4096.
+
+value = GEMM FLOPs of the step / step time (TFLOP/s, the quantisation time
+included).  The quantiser's own GB/s and the per-kernel roofline fractions are
+reported beside it.  `--impl reference` times the CPU oracle on a bounded
+sample of the same step instead.
+
+Run: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch with torchrun; every rank runs an independent replica.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantize GB/s and FP8 scaled-GEMM TFLOPS at 1 GB300, % of HBM/FP8 roofline"
+WORKLOAD = ("fp8 training hot path step: per-tensor current-scaling fwd 256x1024x1024 + 13B FFN fwd+bwd "
+            "16384x20480x5120 per-tensor delayed (L=1024, row+col casts) + MXFP8 fwd 16384x28672x8192 "
+            "(row+col casts) + per-block 1x128/128x128 fwd 8192x11008x4096")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio 4.5 / 2.25 PFLOP/s
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ---------------------------------------------------------------- inputs
+
+def make_inputs():
+    import workloads as wl
+    X1, W1 = wl.linear_fwd_current()
+    X5, W5, dY5 = wl.ffn_fwd_bwd()
+    X4, W4 = wl.mxfp8_inputs()
+    X3, W3 = wl.per_block_up_proj()
+    return dict(X1=X1, W1=W1, X5=X5, W5=W5, dY5=dY5, X4=X4, W4=W4, X3=X3, W3=W3)
+
+
+# ------------------------------------------------------------- GPU side
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        loaded = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import scaling_quantization_gemm_gb300 as q
+    from scaling_quantization_gemm_gb300.step import BlockLinearFwd, LinearFwdBwd, PerTensorFwd
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    q.lib()
+
+    t0 = time.time()
+    host = make_inputs()
+    gen_s = time.time() - t0
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    d = {k: to_dev(v) for k, v in host.items()}
+    c1 = PerTensorFwd(d["X1"], d["W1"])
+    c5 = LinearFwdBwd(d["X5"], d["W5"], d["dY5"], history_len=1024)
+    c4 = BlockLinearFwd(d["X4"], d["W4"], mx=True, col=True)
+    c3 = BlockLinearFwd(d["X3"], d["W3"], mx=False, col=False)
+
+    def c5_q(i):
+        x, st, qr, qc = [(c5.X, c5.sx, c5.qx_row, c5.qx_col), (c5.W, c5.sw, c5.qw_row, c5.qw_col),
+                         (c5.dY, c5.sg, c5.qg_row, c5.qg_col)][i]
+
+        def f():
+            if st.steps == 0:
+                from scaling_quantization_gemm_gb300.step import current_scaling
+                current_scaling(x, st)
+            q.fp8_quantize(x, st.fmt, q.TENSOR, scale=st.scale, q_row=qr, q_col=qc, amax=st.amax)
+        return f
+
+    ops = [  # (name, callable, kind, work per call, our kernel launches per call)
+        ("c1_fwd", c1.run, "mixed", 0.0, 7),
+        ("c5_quant_x", c5_q(0), "quant", 4.0 * c5.X.numel(), 1),
+        ("c5_quant_w", c5_q(1), "quant", 4.0 * c5.W.numel(), 1),
+        ("c5_quant_dy", c5_q(2), "quant", 4.0 * c5.dY.numel(), 1),
+        ("c5_fprop", lambda: q.fp8_scaled_gemm(q.FPROP, c5.qx_row, 0, 0, c5.sx.scale_inv, c5.qw_row, 0, 0,
+                                               c5.sw.scale_inv, c5.Y), "gemm_tensor", c5.flops / 3, 1),
+        ("c5_dgrad", lambda: q.fp8_scaled_gemm(q.DGRAD, c5.qg_row, 1, 0, c5.sg.scale_inv, c5.qw_col, 0, 0,
+                                               c5.sw.scale_inv, c5.dX), "gemm_tensor", c5.flops / 3, 1),
+        ("c5_wgrad", lambda: q.fp8_scaled_gemm(q.WGRAD, c5.qg_col, 1, 0, c5.sg.scale_inv, c5.qx_col, 0, 0,
+                                               c5.sx.scale_inv, c5.dW), "gemm_tensor", c5.flops / 3, 1),
+        ("c5_history", c5.advance, "other", 0.0, 3),
+        ("c4_quant", c4.quantize, "quant", float(c4.quant_bytes), 2),
+        ("c4_gemm_mx", c4.gemm, "gemm_blockscaled", c4.flops, 1),
+        ("c3_quant", c3.quantize, "quant", float(c3.quant_bytes), 2),
+        ("c3_gemm_block", c3.gemm, "gemm_blockscaled", c3.flops, 1),
+    ]
+    step_flops = c1.flops + c5.flops + c4.flops + c3.flops
+    quant_bytes = sum(w for _, _, k, w, _ in ops if k == "quant")
+    launches_per_step = sum(n for *_, n in ops)
+
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for _, f, *_ in ops:
+            f()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # --- timed region: device-resident inputs, events around every op ---
+    nops = len(ops)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        start.record(stream)
+        for s in range(args.steps):
+            evs[s][0].record(stream)
+            for i, (_, f, *_) in enumerate(ops):
+                f()
+                evs[s][i + 1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(total_ms, world)
+    per_op = {ops[i][0]: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
+              for i in range(nops)}
+    ms_step = total_ms / args.steps
+    status = [int(c4.status.item()), int(c3.status.item())] + [int(s.status.item()) for s in (c5.sx, c5.sw, c5.sg)]
+
+    # --- end to end: pinned host inputs in, results out, every step ---
+    e2e = run_e2e(args, d, host, ops, stream, c1, c5, c4, c3, step_flops, world)
+
+    pk, pk_src = peaks()
+    long_loop = total_ms > 1500.0
+    bf16_peak = pk["bf16_tflops_sustained" if long_loop else "bf16_tflops"]
+    fp8_peak = bf16_peak * FP8_OVER_BF16
+    tensor_ms = statistics.mean(per_op[n] for n in ("c5_fprop", "c5_dgrad", "c5_wgrad"))
+    tensor_tflops = (c5.flops / 3) / (tensor_ms * 1e-3) / 1e12
+    mx_tflops = c4.flops / (per_op["c4_gemm_mx"] * 1e-3) / 1e12
+    blk_tflops = c3.flops / (per_op["c3_gemm_block"] * 1e-3) / 1e12
+    quant_ms = sum(per_op[n] for n, _, k, *_ in ops if k == "quant")
+    quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9
+    value = step_flops * world / (ms_step * 1e-3) / 1e12
+    traffic = load_traffic("gemm_tensor_kernel")
+    peak_note = f"{'sustained' if long_loop else 'burst'} bf16 x {FP8_OVER_BF16:g} (nominal fp8/bf16), {pk_src}"
+
+    cpu = cpu_baseline(host) if (rank == 0 and not args.no_cpu_baseline) else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (about 2 GB read per step), no flush",
+                   "step_gemm_tflop": round(step_flops / 1e12, 3), "input_gen_s": round(gen_s, 1)},
+        "roofline": {"bound": "tensor", "kernel": "gemm_tensor_kernel (13B FFN fprop/dgrad/wgrad)",
+                     "achieved": round(tensor_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(tensor_tflops / fp8_peak, 4), "peak_source": peak_note,
+                     "traffic": traffic},
+        "roofline_quantizer": {"bound": "hbm", "kernel": "quantize_tile_kernel (all casts of the step)",
+                               "achieved": round(quant_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                               "frac": round(quant_gbs / pk["hbm_gbs"], 4), "peak_source": pk_src,
+                               "algorithmic_bytes_per_step": int(quant_bytes)},
+        "roofline_blockscaled": {"bound": "tensor", "mxfp8_tflops": round(mx_tflops, 1),
+                                 "mxfp8_frac": round(mx_tflops / fp8_peak, 4),
+                                 "per_block_tflops": round(blk_tflops, 1),
+                                 "per_block_frac": round(blk_tflops / fp8_peak, 4)},
+        "breakdown_ms": {k: round(v, 4) for k, v in per_op.items()},
+        "device_status": status,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, d, host, ops, stream, c1, c5, c4, c3, step_flops, world):
+    import torch
+    pinned_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory() for k, v in host.items()}
+    outs = [c1.Y, c5.Y, c5.dX, c5.dW, c4.Y, c3.Y]
+    pinned_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in pinned_out)
+    steps = max(1, min(args.steps, args.e2e_steps))
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        for k, t in pinned_in.items():
+            d[k].copy_(t, non_blocking=True)
+        for _, f, *_ in ops:
+            f()
+        for o, p in zip(outs, pinned_out):
+            p.copy_(o, non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end), world) / steps
+    return {"value": round(step_flops * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 3),
+            "steps": steps}
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if one matches the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "scaling_quantization_gemm_gb300", "csrc", e.get("source", ""))
+    if e.get("source_sha1") and os.path.exists(src):
+        import hashlib
+        if hashlib.sha1(open(src, "rb").read()).hexdigest() != e["source_sha1"]:
+            return None
+    return e.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_step_sample(host, R: int):
+    """The oracle on a bounded sample of the step: for each of the six GEMMs, quantise R operand rows of
+    A and B (per-tensor scales from full-tensor amaxes; block scales on the sampled rows) and compute
+    the R x R block of outputs in fp64.  Returns (flops, seconds)."""
+    import oracle as o
+    t0 = time.time()
+    flops = 0.0
+
+    def tens(x_bits, fmt, margin=0):
+        return o.scale_triple(o.amax(x_bits), fmt, margin)
+
+    def gemm(Aq, fa, ga, sa, Bq, fb, gb, sb):
+        nonlocal flops
+        y, _ = o.gemm_full(Aq, fa, ga, sa, Bq, fb, gb, sb)
+        flops += 2.0 * Aq.shape[0] * Bq.shape[0] * Aq.shape[1]
+        return y
+
+    # per-tensor current scaling fwd
+    X1, W1 = host["X1"], host["W1"]
+    _, s1x, i1x = tens(X1, 0)
+    _, s1w, i1w = tens(W1, 0)
+    gemm(o.quantize_tensor(X1[:R], 0, s1x)[0], 0, 0, i1x, o.quantize_tensor(W1[:R], 0, s1w)[0], 0, 0, i1w)
+    # FFN fwd + bwd, per-tensor
+    X5, W5, dY5 = host["X5"], host["W5"], host["dY5"]
+    _, sx, ix = tens(X5, 0)
+    _, sw, iw = tens(W5, 0)
+    _, sg, ig = tens(dY5, 1)
+    qx = o.quantize_tensor(X5[:R], 0, sx)[0]
+    qw = o.quantize_tensor(W5[:R], 0, sw)[0]
+    gemm(qx, 0, 0, ix, qw, 0, 0, iw)
+    qg = o.quantize_tensor(dY5[:R], 1, sg)[0]
+    qwc = o.quantize_tensor(np.ascontiguousarray(W5[:, :R]), 0, sw, row=False, col=True)[1]
+    gemm(qg, 1, 0, ig, qwc, 0, 0, iw)
+    qgc = o.quantize_tensor(np.ascontiguousarray(dY5[:, :R]), 1, sg, row=False, col=True)[1]
+    qxc = o.quantize_tensor(np.ascontiguousarray(X5[:, :R]), 0, sx, row=False, col=True)[1]
+    gemm(qgc, 1, 0, ig, qxc, 0, 0, ix)
+    # MXFP8
+    qa, sa, _, _, _ = o.quantize_block(host["X4"][:R], 0, o.MX_1x32)
+    qb, sb, _, _, _ = o.quantize_block(host["W4"][:R], 0, o.MX_1x32)
+    gemm(qa, 0, 3, sa, qb, 0, 3, sb)
+    # per-block
+    qa, sa, _, _, _ = o.quantize_block(host["X3"][:R], 0, o.BLOCK_1x128)
+    qb, sb, _, _, _ = o.quantize_block(host["W3"][:R], 0, o.BLOCK_128x128)
+    gemm(qa, 0, 1, sa, qb, 0, 2, sb)
+    return flops, time.time() - t0
+
+
+def cpu_baseline(host, R: int = 256):
+    import oracle as o
+    o.lib()
+    flops, sec = oracle_step_sample(host, R)
+    return {"value": round(flops / sec / 1e12, 6), "unit": "TFLOP/s", "cores": o.max_threads(), "kind": "oracle",
+            "sample": f"{R}x{R} output block of each of the 6 GEMMs of the step, operand rows quantised by the "
+                      f"oracle (per-tensor scales from full-tensor amax); {flops / 1e9:.2f} GFLOP in {sec:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle as o
+    o.lib()
+    host = make_inputs()
+    R = args.reference_rows
+    for _ in range(args.warmup):
+        oracle_step_sample(host, R)
+    tot_f, tot_s = 0.0, 0.0
+    for _ in range(args.steps):
+        f, s = oracle_step_sample(host, R)
+        tot_f += f
+        tot_s += s
+    v = tot_f / tot_s / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_s / args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": f"{R}x{R} output block per GEMM"},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": o.max_threads(), "kind": "oracle",
+                         "sample": f"{R}x{R} output block of each of the 6 GEMMs per step"},
+        "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# -------------------------------------------------------------- plumbing
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--reference-rows", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world)
+    if world > 1 and args.impl != "reference":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * fp8q.h -- C ABI of the FP8 amax / scale-selection / scaled-cast / scaled-GEMM
+ * library for one GB300 GPU (sm_103a).
+ *
+ * The method (papers and posts cited by title and section):
+ *   - per-tensor scaling with the FP8-AMAX rule: a bias per tensor from the
+ *     tensor's maximum absolute value, e = floor(log2(fmax/amax)) - margin
+ *     ("Training and inference of large language models using 8-bit floating
+ *     point", section "Proposed method");
+ *   - the operands are multiplied by their scales before the FP8 cast and the
+ *     matrix product is divided by them afterwards (same section);
+ *   - FP8_E4 (E4M3) for weights and activations, FP8_E5 (E5M2) for gradients
+ *     (same section);
+ *   - delayed scaling from the maximum amax over a window of past iterations,
+ *     and per-block / MXFP8 scaling with one scale per block ("Per-Tensor and
+ *     Per-Block Scaling Strategies for Effective FP8 Training", "Key Questions
+ *     Answered").
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument that names a tensor is a DEVICE pointer into memory
+ *     the caller allocated and owns.  The library allocates no device memory,
+ *     keeps no global state between calls, and is safe to call from several
+ *     host threads on different streams.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *     only enqueues work on that stream and returns; none synchronises the host.
+ *   - Arguments are validated on the host before anything is enqueued:
+ *     a NULL required pointer, a negative size or an inconsistent leading
+ *     dimension returns FP8_ERR_INVALID_ARG; a shape or alignment the kernels do
+ *     not handle returns FP8_ERR_UNSUPPORTED (never a silent slow path).  A
+ *     failed launch returns FP8_ERR_CUDA.  A size of zero is a valid no-op.
+ *   - Conditions only the device can see (a non-finite amax, a non-power-of-two
+ *     block scale, an internal wait that gave up) are ORed as bits into an
+ *     optional device status word (`status`, int32, may be NULL); kernels never
+ *     trap.
+ *   - bf16 inputs are row-major [rows x cols] with leading dimension `ld`
+ *     (elements, ld >= cols).  FP8 outputs are one byte per element, OFP8 E4M3
+ *     or E5M2 bit patterns, row-major and dense.
+ *   - Scales are powers of two.  A per-tensor quantisation scale is the
+ *     multiplier s = 2^e applied before the cast; the GEMM takes the
+ *     dequantisation factor s^-1 = 2^-e.  Block scales are stored as
+ *     dequantisation factors (fp32 2^-e, or the E8M0 code 127 - e).
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+
+/* Symbols of the C ABI are the only ones the shared library exports. */
+#if defined(__GNUC__)
+#define FP8Q_API __attribute__((visibility("default")))
+#else
+#define FP8Q_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8_OK = 0,
+    FP8_ERR_INVALID_ARG = 1,
+    FP8_ERR_UNSUPPORTED = 2,
+    FP8_ERR_CUDA = 3,
+    FP8_ERR_TIMEOUT = 4
+} fp8_status;
+
+typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format;
+
+typedef enum {
+    FP8_SCALE_TENSOR = 0,        /* one scale for the whole tensor */
+    FP8_SCALE_BLOCK_1x128 = 1,   /* activation blocks: 1 row x 128 columns */
+    FP8_SCALE_BLOCK_128x128 = 2, /* weight blocks: 128 x 128 */
+    FP8_SCALE_MX_1x32 = 3        /* MXFP8: 1 x 32 blocks, E8M0 scales */
+} fp8_granularity;
+
+typedef enum { FP8_GEMM_FPROP = 0, FP8_GEMM_DGRAD = 1, FP8_GEMM_WGRAD = 2 } fp8_gemm_op;
+
+typedef enum { FP8_OUT_F32 = 0, FP8_OUT_BF16 = 1 } fp8_out_dtype;
+
+/* Bits of the device status word. */
+#define FP8_STATUS_NONFINITE_AMAX 1  /* an amax was NaN or Inf; its bias was set to 0 */
+#define FP8_STATUS_TIMEOUT 2         /* a bounded wait inside a kernel gave up; output invalid */
+#define FP8_STATUS_BAD_BLOCK_SCALE 4 /* a block scale given to the GEMM was not a power of two */
+
+/*
+ * fp8_amax -- maximum absolute value of a bf16 tensor.
+ * Source: the per-tensor statistic the FP8-AMAX scales are computed from
+ * ("Training and inference of large language models using 8-bit floating
+ * point", "Proposed method").
+ *
+ *   x      device, bf16 [rows x cols], leading dimension ld (elements), 16-byte
+ *          aligned; cols and ld must be multiples of 8 (else UNSUPPORTED).
+ *   amax   device, one fp32.  ACCUMULATED: the call stores max(*amax, max|x|),
+ *          so the caller zeroes it first (fp8_amax_history_update resets it).
+ *          A NaN anywhere in x makes the result NaN.
+ */
+FP8Q_API fp8_status fp8_amax(const void *x, int64_t rows, int64_t cols, int64_t ld, float *amax, void *stream);
+
+/*
+ * fp8_compute_scale -- the FP8-AMAX compute_bias rule for current scaling.
+ * Source: the compute_bias rule of FP8-AMAX, a base-2 logarithm of the format
+ * maximum over the tensor's amax less a margin ("Training and inference of
+ * large language models using 8-bit floating point", "Proposed method").
+ *
+ *   e = floor(log2(fmax / amax)) - margin, fmax = 448 (E4M3) or 57344 (E5M2),
+ *   computed exactly from the exponent and mantissa bits of amax, clamped to
+ *   [-126, 127].  amax == 0 gives e = 0; a non-finite amax gives e = 0 and sets
+ *   FP8_STATUS_NONFINITE_AMAX.
+ *
+ *   amax       device, one fp32 (read).
+ *   bias       device, one int32 (written: e).          May be NULL.
+ *   scale      device, one fp32 (written: 2^e).          May be NULL.
+ *   scale_inv  device, one fp32 (written: 2^-e).         May be NULL.
+ *   status     device, one int32 (bits ORed in).         May be NULL.
+ */
+FP8Q_API fp8_status fp8_compute_scale(const float *amax, fp8_format fmt, int32_t margin, int32_t *bias, float *scale,
+                             float *scale_inv, int32_t *status, void *stream);
+
+/*
+ * fp8_amax_history_update -- one delayed-scaling step.
+ * Source: delayed scaling, where the scale comes from the largest amax seen
+ * in a window of past steps ("Per-Tensor and Per-Block Scaling Strategies for
+ * Effective FP8 Training", "Key Questions Answered").
+ *
+ *   history[pos mod len] = *amax;  pos += 1;
+ *   e = compute_bias(max(history[0 .. min(pos, len) - 1]), fmt, margin);
+ *   bias = e; scale = 2^e; scale_inv = 2^-e;  *amax = 0.
+ *
+ *   history    device, fp32[len], zero-initialised by the caller before step 0.
+ *   len        window length, 1 <= len <= 65536.
+ *   pos        device, one int64 (read and incremented).
+ *   amax       device, one fp32 (read, then reset to 0 for the next step).
+ *   bias, scale, scale_inv, status: as for fp8_compute_scale (bias/scale/
+ *              scale_inv required here).
+ * The state (history, pos, bias, scale, scale_inv) is plain device memory:
+ * copying it out and back in resumes the sequence exactly.
+ */
+FP8Q_API fp8_status fp8_amax_history_update(float *history, int32_t len, int64_t *pos, float *amax, fp8_format fmt,
+                                   int32_t margin, int32_t *bias, float *scale, float *scale_inv,
+                                   int32_t *status, void *stream);
+
+/*
+ * fp8_quantize -- the scaled cast to FP8, row-wise and/or column-wise.
+ * Source: the scaling step that precedes the FP8 cast ("Training and
+ * inference of large language models using 8-bit floating point", "Proposed
+ * method");
+ * per-block and MXFP8 block scales ("Per-Tensor and Per-Block Scaling
+ * Strategies for Effective FP8 Training", "Key Questions Answered").
+ *
+ *   q = RNE_saturate_fmt(x * 2^e) with the product taken in fp32.
+ *
+ *   x        device, bf16 [rows x cols], leading dimension ld; 16-byte aligned,
+ *            cols and ld multiples of 8.
+ *   gran     FP8_SCALE_TENSOR: e from `scale` (device fp32 2^e, required);
+ *              sf_row and sf_col must be NULL.
+ *            FP8_SCALE_BLOCK_1x128 / _128x128 / FP8_SCALE_MX_1x32: each block
+ *              gets e_b = compute_bias(amax_b, fmt, margin); `scale` must be NULL.
+ *              A partial block at an edge uses the elements that exist.
+ *   margin   used by the block granularities only.
+ *   q_row    device u8 [rows x cols] (dense), or NULL.
+ *   q_col    device u8 [cols x rows] (dense, the transposed copy), or NULL.
+ *            At least one of q_row / q_col.  With q_col, rows must be a
+ *            multiple of 16.  The column-wise copy is the row-wise
+ *            quantisation of x transposed: per-tensor and 128x128 use the same
+ *            scales as row-wise; 1x128 becomes 128x1 blocks down each column and
+ *            MX 1x32 becomes 32x1.
+ *   sf_row   block scales of q_row (required iff q_row and gran != TENSOR):
+ *              1x128:   fp32 [rows x ceil(cols/128)]
+ *              128x128: fp32 [ceil(rows/128) x ceil(cols/128)]
+ *              MX 1x32: u8 E8M0 [rows x ceil(cols/32)]
+ *   sf_col   block scales of q_col (required iff q_col and gran != TENSOR):
+ *              1x128:   fp32 [cols x ceil(rows/128)]
+ *              128x128: fp32 [ceil(cols/128) x ceil(rows/128)]
+ *              MX 1x32: u8 E8M0 [cols x ceil(rows/32)]
+ *            Stored values are dequantisation factors 2^-e_b (fp32) or 127-e_b.
+ *   amax     device fp32 or NULL: if given, max|x| is accumulated into it
+ *            (fused amax for delayed scaling; same semantics as fp8_amax).
+ */
+FP8Q_API fp8_status fp8_quantize(const void *x, int64_t rows, int64_t cols, int64_t ld, fp8_format fmt,
+                        fp8_granularity gran, int32_t margin, const float *scale, uint8_t *q_row, uint8_t *q_col,
+                        void *sf_row, void *sf_col, float *amax, void *stream);
+
+/*
+ * fp8_scaled_gemm -- D = unscale(A . B^T) on FP8 operands.
+ * Source: the unscaling step that follows the FP8 matrix product ("Training
+ * and inference of large language models using 8-bit floating point",
+ * "Proposed method"); block
+ * and MXFP8 scales ("Per-Tensor and Per-Block Scaling Strategies for Effective
+ * FP8 Training", "Key Questions Answered").
+ *
+ *   D[m, n] = sum_k (A[m,k] sa(m,k)) (B[n,k] sb(n,k)),  fp32 accumulation.
+ *
+ *   op       FPROP (A = X_row, B = W_row), DGRAD (A = dY_row, B = W_col) or
+ *            WGRAD (A = dY_col, B = X_col).  Every op is the same TN product
+ *            over K-major operands; op only labels the call.
+ *   A        device u8 [M x K], leading dimension lda (bytes), format fa.
+ *   B        device u8 [N x K], leading dimension ldb (bytes), format fb.
+ *            A and B 16-byte aligned; K, lda and ldb multiples of 16.
+ *   ga, gb   scale granularity of A and of B:
+ *              both FP8_SCALE_TENSOR: sfa / sfb point to ONE fp32 each, the
+ *                dequantisation factor 2^-e of that tensor;
+ *              otherwise neither may be TENSOR, and each of sfa / sfb is
+ *                1x128:   fp32 [rows x ceil(K/128)]
+ *                128x128: fp32 [ceil(rows/128) x ceil(K/128)]
+ *                MX 1x32: u8 E8M0 [rows x ceil(K/32)] (K must be a multiple of 32)
+ *              (rows = M for A, N for B).  fp32 block scales must be powers of
+ *              two in [2^-127, 2^127] (what fp8_quantize writes); any other
+ *              value sets FP8_STATUS_BAD_BLOCK_SCALE.
+ *   D        device, [M x N] fp32 or bf16 (out_dtype), leading dimension ldd
+ *            (elements); 16-byte aligned, N and ldd multiples of 16.
+ *   status   device int32 or NULL (FP8_STATUS_TIMEOUT, FP8_STATUS_BAD_BLOCK_SCALE).
+ * K == 0 writes zeros.  Block-scaled modes need M, N >= 1 and K >= 32.
+ */
+FP8Q_API fp8_status fp8_scaled_gemm(fp8_gemm_op op, int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda,
+                           fp8_format fa, fp8_granularity ga, const void *sfa, const uint8_t *B, int64_t ldb,
+                           fp8_format fb, fp8_granularity gb, const void *sfb, void *D, fp8_out_dtype out_dtype,
+                           int64_t ldd, int32_t *status, void *stream);
+
+/* fp8_status_string -- static, human-readable name of a status code. */
+FP8Q_API const char *fp8_status_string(fp8_status s);
+
+/* fp8_last_error_detail -- static text describing the last non-OK status
+ * returned on the calling host thread (thread-local; empty if none). */
+FP8Q_API const char *fp8_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

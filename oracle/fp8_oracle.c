@@ -18,8 +18,8 @@
  *    the midpoints between neighbouring representable values.
  *
  *  - compute_bias: the per-tensor exponent bias is floor(log2(fmax/amax)) minus
- *    a configurable margin (same page, "Proposed method": a bias computed from
- *    log2 of format maximum over tensor amplitude, with a margin).
+ *    a margin (same page, "Proposed method": the bias is the base-2 logarithm
+ *    of the format maximum over the tensor's amax, less a margin).
  *
  *  - quantise: scale before the cast (same page, "Proposed method"): q =
  *    Encode(x * 2^e), the product taken in fp32, the precision of the kernels.
@@ -30,11 +30,10 @@
  *
  *  - delayed scaling: the scale for the next step comes from the maximum of the
  *    amax values recorded over the last L steps (first page, "Key Questions
- *    Answered": delayed scaling from maximum absolute values over several
- *    iterations).
+ *    Answered": the delayed scale looks back over a window of past steps).
  *
- *  - GEMM: the exact fp64 product of the dequantised operands, "unscale after
- *    matrix multiplication" (second page, "Proposed method").
+ *  - GEMM: the exact fp64 product of the dequantised operands: the FP8 product
+ *    is unscaled after the multiplication (second page, "Proposed method").
  *
  * Compile with -ffp-contract=off and without -ffast-math.
  */

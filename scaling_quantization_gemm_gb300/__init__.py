@@ -1,0 +1,157 @@
+"""GB300-native FP8 amax / scale selection / scaled cast / scaled GEMM.
+
+A thin ctypes binding over ``libfp8q.so`` (``include/fp8q.h``).  Every function
+has the name of the C entry point it calls and only marshals arguments: it
+reads shapes, strides and data pointers from torch tensors (or takes raw device
+pointers as ints), passes the caller's current CUDA stream, and raises
+``FP8Error`` on a non-OK status.  All computation runs in the library's CUDA
+kernels; there is no other code path.  If the library is not built, importing
+works but every call raises.
+
+Build it with ``python -m scaling_quantization_gemm_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Union
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfp8q.so")
+
+# enums of include/fp8q.h
+FP8_OK, FP8_ERR_INVALID_ARG, FP8_ERR_UNSUPPORTED, FP8_ERR_CUDA, FP8_ERR_TIMEOUT = 0, 1, 2, 3, 4
+E4M3, E5M2 = 0, 1
+TENSOR, BLOCK_1x128, BLOCK_128x128, MX_1x32 = 0, 1, 2, 3
+FPROP, DGRAD, WGRAD = 0, 1, 2
+OUT_F32, OUT_BF16 = 0, 1
+STATUS_NONFINITE_AMAX, STATUS_TIMEOUT, STATUS_BAD_BLOCK_SCALE = 1, 2, 4
+
+# every entry point declared in include/fp8q.h
+ENTRY_POINTS = ("fp8_amax", "fp8_compute_scale", "fp8_amax_history_update", "fp8_quantize", "fp8_scaled_gemm",
+                "fp8_status_string", "fp8_last_error_detail")
+
+
+class FP8Error(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str):
+        super().__init__(f"{fn}: {status_name(status)}: {detail}")
+        self.status = status
+        self.detail = detail
+
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libfp8q.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is not built; run `python -m scaling_quantization_gemm_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+            for name, args in {
+                "fp8_amax": [vp, i64, i64, i64, vp, vp],
+                "fp8_compute_scale": [vp, i32, i32, vp, vp, vp, vp, vp],
+                "fp8_amax_history_update": [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp],
+                "fp8_quantize": [vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp],
+                "fp8_scaled_gemm": [i32, i64, i64, i64, vp, i64, i32, i32, vp, vp, i64, i32, i32, vp, vp, i32, i64,
+                                    vp, vp],
+            }.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = ctypes.c_int
+            L.fp8_status_string.argtypes = [ctypes.c_int]
+            L.fp8_status_string.restype = ctypes.c_char_p
+            L.fp8_last_error_detail.argtypes = []
+            L.fp8_last_error_detail.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def status_name(s: int) -> str:
+    return lib().fp8_status_string(int(s)).decode()
+
+
+Ptr = Union[None, int, torch.Tensor]
+
+
+def _p(t: Ptr) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return t.data_ptr() if t.numel() > 0 else None
+    return int(t)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        if torch.cuda.is_available():
+            return torch.cuda.current_stream().cuda_stream or None
+        return None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn: str, st: int) -> None:
+    if st != FP8_OK:
+        raise FP8Error(fn, st, lib().fp8_last_error_detail().decode())
+
+
+def _matrix(x: torch.Tensor):
+    if x.dim() != 2 or (x.size(1) > 1 and x.stride(1) != 1):
+        raise ValueError("expected a 2-D row-major tensor (unit column stride)")
+    return x.size(0), x.size(1), x.stride(0) if x.size(0) > 1 else max(x.size(1), 1)
+
+
+def fp8_amax(x: torch.Tensor, amax: Ptr, stream=None) -> None:
+    """amax <- max(amax, max|x|) for a bf16 [rows x cols] tensor (see fp8_amax in fp8q.h)."""
+    rows, cols, ld = _matrix(x)
+    _check("fp8_amax", lib().fp8_amax(_p(x), rows, cols, ld, _p(amax), _stream(stream)))
+
+
+def fp8_compute_scale(amax: Ptr, fmt: int, margin: int, bias: Ptr = None, scale: Ptr = None,
+                      scale_inv: Ptr = None, status: Ptr = None, stream=None) -> None:
+    _check("fp8_compute_scale", lib().fp8_compute_scale(_p(amax), fmt, margin, _p(bias), _p(scale), _p(scale_inv),
+                                                        _p(status), _stream(stream)))
+
+
+def fp8_amax_history_update(history: torch.Tensor, pos: Ptr, amax: Ptr, fmt: int, margin: int, bias: Ptr,
+                            scale: Ptr, scale_inv: Ptr, status: Ptr = None, stream=None) -> None:
+    _check("fp8_amax_history_update",
+           lib().fp8_amax_history_update(_p(history), history.numel(), _p(pos), _p(amax), fmt, margin, _p(bias),
+                                         _p(scale), _p(scale_inv), _p(status), _stream(stream)))
+
+
+def fp8_quantize(x: torch.Tensor, fmt: int, gran: int, margin: int = 0, scale: Ptr = None, q_row: Ptr = None,
+                 q_col: Ptr = None, sf_row: Ptr = None, sf_col: Ptr = None, amax: Ptr = None, stream=None) -> None:
+    rows, cols, ld = _matrix(x)
+    _check("fp8_quantize", lib().fp8_quantize(_p(x), rows, cols, ld, fmt, gran, margin, _p(scale), _p(q_row),
+                                              _p(q_col), _p(sf_row), _p(sf_col), _p(amax), _stream(stream)))
+
+
+def fp8_scaled_gemm(op: int, A: torch.Tensor, fa: int, ga: int, sfa: Ptr, B: torch.Tensor, fb: int, gb: int,
+                    sfb: Ptr, D: torch.Tensor, status: Ptr = None, stream=None) -> None:
+    """D[M x N] = unscale(A[M x K] . B[N x K]^T); out dtype from D (float32 or bfloat16)."""
+    M, K, lda = _matrix(A)
+    N, K2, ldb = _matrix(B)
+    if K != K2:
+        raise ValueError("A and B disagree on K")
+    Dm, Dn, ldd = _matrix(D)
+    if (Dm, Dn) != (M, N):
+        raise ValueError("D must be [M x N]")
+    out = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}[D.dtype]
+    _check("fp8_scaled_gemm", lib().fp8_scaled_gemm(op, M, N, K, _p(A), lda, fa, ga, _p(sfa), _p(B), ldb, fb, gb,
+                                                    _p(sfb), _p(D), out, ldd, _p(status), _stream(stream)))
+
+
+__all__ = ["lib", "FP8Error", "status_name", "fp8_amax", "fp8_compute_scale", "fp8_amax_history_update",
+           "fp8_quantize", "fp8_scaled_gemm", "ENTRY_POINTS", "LIB_PATH", "E4M3", "E5M2", "TENSOR", "BLOCK_1x128",
+           "BLOCK_128x128", "MX_1x32", "FPROP", "DGRAD", "WGRAD", "OUT_F32", "OUT_BF16"]

@@ -1,0 +1,177 @@
+// api.cu -- the extern "C" entry points of libfp8q: argument validation on the
+// host, then one or more asynchronous launches on the caller's stream.
+// Declarations, argument meaning, layouts and error behaviour: include/fp8q.h.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace fp8q {
+
+static thread_local char g_detail[512];
+
+void set_error_detail(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_detail, sizeof g_detail, fmt, ap);
+    va_end(ap);
+}
+
+fp8_status launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* amax, cudaStream_t st);
+fp8_status launch_compute_scale(const float* amax, int fmt, int margin, int32_t* bias, float* scale, float* scale_inv,
+                                int32_t* status, cudaStream_t st);
+fp8_status launch_history(float* hist, int len, int64_t* pos, float* amax, int fmt, int margin, int32_t* bias,
+                          float* scale, float* scale_inv, int32_t* status, cudaStream_t st);
+fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int gran, int margin,
+                           const float* scale, uint8_t* q_row, uint8_t* q_col, void* sf_row, void* sf_col,
+                           float* amax, cudaStream_t st);
+fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, int fa, int ga, const void* sfa,
+                       const uint8_t* B, int64_t ldb, int fb, int gb, const void* sfb, void* D, int out_bf16,
+                       int64_t ldd, int32_t* status, cudaStream_t st);
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool valid_fmt(int f) { return f == FP8_E4M3 || f == FP8_E5M2; }
+bool valid_gran(int g) { return g >= FP8_SCALE_TENSOR && g <= FP8_SCALE_MX_1x32; }
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+fp8_status check_bf16_matrix(const void* x, int64_t rows, int64_t cols, int64_t ld) {
+    FP8_REQUIRE(rows >= 0 && cols >= 0, FP8_ERR_INVALID_ARG, "negative size (rows=%lld cols=%lld)", (long long)rows,
+                (long long)cols);
+    FP8_REQUIRE(ld >= cols && ld >= 1, FP8_ERR_INVALID_ARG, "ld (%lld) < cols (%lld)", (long long)ld, (long long)cols);
+    if (rows == 0 || cols == 0) return FP8_OK;
+    FP8_REQUIRE(x != nullptr, FP8_ERR_INVALID_ARG, "x is NULL");
+    FP8_REQUIRE(cols % 8 == 0 && ld % 8 == 0, FP8_ERR_UNSUPPORTED, "cols and ld must be multiples of 8 (16-byte rows)");
+    FP8_REQUIRE(aligned(x, 16), FP8_ERR_UNSUPPORTED, "x must be 16-byte aligned");
+    return FP8_OK;
+}
+
+}  // namespace
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" {
+
+const char* fp8_status_string(fp8_status s) {
+    switch (s) {
+        case FP8_OK: return "FP8_OK";
+        case FP8_ERR_INVALID_ARG: return "FP8_ERR_INVALID_ARG";
+        case FP8_ERR_UNSUPPORTED: return "FP8_ERR_UNSUPPORTED";
+        case FP8_ERR_CUDA: return "FP8_ERR_CUDA";
+        case FP8_ERR_TIMEOUT: return "FP8_ERR_TIMEOUT";
+    }
+    return "FP8_ERR_UNKNOWN";
+}
+
+const char* fp8_last_error_detail(void) { return g_detail; }
+
+fp8_status fp8_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* amax, void* stream) {
+    g_detail[0] = 0;
+    fp8_status s = check_bf16_matrix(x, rows, cols, ld);
+    if (s != FP8_OK) return s;
+    FP8_REQUIRE(amax != nullptr, FP8_ERR_INVALID_ARG, "amax is NULL");
+    FP8_REQUIRE(aligned(amax, 4), FP8_ERR_INVALID_ARG, "amax must be 4-byte aligned");
+    if (rows == 0 || cols == 0) return FP8_OK;
+    return launch_amax(x, rows, cols, ld, amax, as_stream(stream));
+}
+
+fp8_status fp8_compute_scale(const float* amax, fp8_format fmt, int32_t margin, int32_t* bias, float* scale,
+                             float* scale_inv, int32_t* status, void* stream) {
+    g_detail[0] = 0;
+    FP8_REQUIRE(amax != nullptr, FP8_ERR_INVALID_ARG, "amax is NULL");
+    FP8_REQUIRE(valid_fmt(fmt), FP8_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
+    FP8_REQUIRE(bias || scale || scale_inv, FP8_ERR_INVALID_ARG, "no output (bias, scale, scale_inv all NULL)");
+    return launch_compute_scale(amax, fmt, margin, bias, scale, scale_inv, status, as_stream(stream));
+}
+
+fp8_status fp8_amax_history_update(float* history, int32_t len, int64_t* pos, float* amax, fp8_format fmt,
+                                   int32_t margin, int32_t* bias, float* scale, float* scale_inv, int32_t* status,
+                                   void* stream) {
+    g_detail[0] = 0;
+    FP8_REQUIRE(history && pos && amax && bias && scale && scale_inv, FP8_ERR_INVALID_ARG,
+                "history, pos, amax, bias, scale and scale_inv are required");
+    FP8_REQUIRE(len >= 1 && len <= 65536, FP8_ERR_INVALID_ARG, "len must be in [1, 65536] (got %d)", (int)len);
+    FP8_REQUIRE(valid_fmt(fmt), FP8_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
+    FP8_REQUIRE(aligned(pos, 8), FP8_ERR_INVALID_ARG, "pos must be 8-byte aligned");
+    return launch_history(history, len, pos, amax, fmt, margin, bias, scale, scale_inv, status, as_stream(stream));
+}
+
+fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, fp8_format fmt, fp8_granularity gran,
+                        int32_t margin, const float* scale, uint8_t* q_row, uint8_t* q_col, void* sf_row,
+                        void* sf_col, float* amax, void* stream) {
+    g_detail[0] = 0;
+    fp8_status s = check_bf16_matrix(x, rows, cols, ld);
+    if (s != FP8_OK) return s;
+    FP8_REQUIRE(valid_fmt(fmt), FP8_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
+    FP8_REQUIRE(valid_gran(gran), FP8_ERR_INVALID_ARG, "unknown granularity %d", (int)gran);
+    if (rows == 0 || cols == 0) return FP8_OK;
+    FP8_REQUIRE(q_row || q_col, FP8_ERR_INVALID_ARG, "q_row and q_col are both NULL");
+    if (gran == FP8_SCALE_TENSOR) {
+        FP8_REQUIRE(scale != nullptr, FP8_ERR_INVALID_ARG, "per-tensor quantisation needs scale");
+        FP8_REQUIRE(!sf_row && !sf_col, FP8_ERR_INVALID_ARG, "per-tensor quantisation takes no block scales");
+    } else {
+        FP8_REQUIRE(scale == nullptr, FP8_ERR_INVALID_ARG, "block quantisation takes no per-tensor scale");
+        FP8_REQUIRE(!q_row || sf_row, FP8_ERR_INVALID_ARG, "q_row needs sf_row");
+        FP8_REQUIRE(!q_col || sf_col, FP8_ERR_INVALID_ARG, "q_col needs sf_col");
+        FP8_REQUIRE(!sf_row || q_row, FP8_ERR_INVALID_ARG, "sf_row given without q_row");
+        FP8_REQUIRE(!sf_col || q_col, FP8_ERR_INVALID_ARG, "sf_col given without q_col");
+        const uintptr_t sa = gran == FP8_SCALE_MX_1x32 ? 1 : 4;
+        FP8_REQUIRE((!sf_row || aligned(sf_row, sa)) && (!sf_col || aligned(sf_col, sa)), FP8_ERR_INVALID_ARG,
+                    "block scale tensors must be aligned to their element size");
+    }
+    FP8_REQUIRE(!amax || aligned(amax, 4), FP8_ERR_INVALID_ARG, "amax must be 4-byte aligned");
+    FP8_REQUIRE(!q_row || aligned(q_row, 8), FP8_ERR_UNSUPPORTED, "q_row must be 8-byte aligned");
+    if (q_col) {
+        FP8_REQUIRE(rows % 16 == 0, FP8_ERR_UNSUPPORTED, "column-wise output needs rows %% 16 == 0 (rows=%lld)",
+                    (long long)rows);
+        FP8_REQUIRE(aligned(q_col, 16), FP8_ERR_UNSUPPORTED, "q_col must be 16-byte aligned");
+    }
+    return launch_quantize(x, rows, cols, ld, fmt, gran, margin, scale, q_row, q_col, sf_row, sf_col, amax,
+                           as_stream(stream));
+}
+
+fp8_status fp8_scaled_gemm(fp8_gemm_op op, int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                           fp8_format fa, fp8_granularity ga, const void* sfa, const uint8_t* B, int64_t ldb,
+                           fp8_format fb, fp8_granularity gb, const void* sfb, void* D, fp8_out_dtype out_dtype,
+                           int64_t ldd, int32_t* status, void* stream) {
+    g_detail[0] = 0;
+    FP8_REQUIRE(op == FP8_GEMM_FPROP || op == FP8_GEMM_DGRAD || op == FP8_GEMM_WGRAD, FP8_ERR_INVALID_ARG,
+                "unknown gemm op %d", (int)op);
+    FP8_REQUIRE(M >= 0 && N >= 0 && K >= 0, FP8_ERR_INVALID_ARG, "negative size");
+    FP8_REQUIRE(valid_fmt(fa) && valid_fmt(fb), FP8_ERR_INVALID_ARG, "unknown format");
+    FP8_REQUIRE(valid_gran(ga) && valid_gran(gb), FP8_ERR_INVALID_ARG, "unknown granularity");
+    FP8_REQUIRE(out_dtype == FP8_OUT_F32 || out_dtype == FP8_OUT_BF16, FP8_ERR_INVALID_ARG, "unknown output dtype");
+    FP8_REQUIRE((ga == FP8_SCALE_TENSOR) == (gb == FP8_SCALE_TENSOR), FP8_ERR_INVALID_ARG,
+                "per-tensor scaling must be used for both operands or for neither");
+    FP8_REQUIRE(ldd >= N, FP8_ERR_INVALID_ARG, "ldd < N");
+    if (M == 0 || N == 0) return FP8_OK;
+    FP8_REQUIRE(D != nullptr, FP8_ERR_INVALID_ARG, "D is NULL");
+    const int esz = out_dtype == FP8_OUT_F32 ? 4 : 2;
+    FP8_REQUIRE(N % 16 == 0 && ldd % 16 == 0, FP8_ERR_UNSUPPORTED, "N and ldd must be multiples of 16");
+    FP8_REQUIRE(aligned(D, 16), FP8_ERR_UNSUPPORTED, "D must be 16-byte aligned");
+    FP8_REQUIRE(M < (1ll << 31) && N < (1ll << 31) && K < (1ll << 31), FP8_ERR_UNSUPPORTED, "dimension >= 2^31");
+    if (K == 0) {
+        cudaError_t e = cudaMemset2DAsync(D, (size_t)ldd * esz, 0, (size_t)N * esz, (size_t)M, as_stream(stream));
+        FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaMemset2DAsync: %s", cudaGetErrorString(e));
+        return FP8_OK;
+    }
+    FP8_REQUIRE(A != nullptr && B != nullptr, FP8_ERR_INVALID_ARG, "A or B is NULL");
+    FP8_REQUIRE(sfa != nullptr && sfb != nullptr, FP8_ERR_INVALID_ARG, "sfa and sfb are required");
+    FP8_REQUIRE(lda >= K && ldb >= K, FP8_ERR_INVALID_ARG, "lda/ldb < K");
+    FP8_REQUIRE(K % 16 == 0 && lda % 16 == 0 && ldb % 16 == 0, FP8_ERR_UNSUPPORTED,
+                "K, lda and ldb must be multiples of 16");
+    FP8_REQUIRE(aligned(A, 16) && aligned(B, 16), FP8_ERR_UNSUPPORTED, "A and B must be 16-byte aligned");
+    if (ga != FP8_SCALE_TENSOR) {
+        FP8_REQUIRE(K % 128 == 0, FP8_ERR_UNSUPPORTED, "block-scaled GEMM needs K %% 128 == 0");
+        FP8_REQUIRE(aligned(sfa, 4) && aligned(sfb, 4), FP8_ERR_UNSUPPORTED, "scale tensors must be 4-byte aligned");
+    } else {
+        FP8_REQUIRE(aligned(sfa, 4) && aligned(sfb, 4), FP8_ERR_INVALID_ARG, "sfa/sfb must be 4-byte aligned");
+    }
+    return launch_gemm(M, N, K, A, lda, fa, ga, sfa, B, ldb, fb, gb, sfb, D, out_dtype == FP8_OUT_BF16, ldd, status,
+                       as_stream(stream));
+}
+
+}  // extern "C"

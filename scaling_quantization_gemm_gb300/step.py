@@ -1,0 +1,204 @@
+"""Host-side sequencing of the FP8 hot path over the C entry points.
+
+Nothing here computes: each function enqueues library kernels on the current
+CUDA stream in the method's order: scale, cast to FP8, multiply, unscale
+("Training and inference of large language models using 8-bit floating
+point", "Proposed method").  Device
+buffers are torch tensors; torch is only the allocator.
+
+* ``ScaleState`` holds one tensor's scaling state on the device: the amax
+  accumulator, bias, scale 2^e and scale_inv 2^-e, plus the amax history ring
+  and its position for delayed scaling.
+* ``current_scaling`` runs amax -> compute_scale (the FP8-AMAX rule).
+* ``LinearFwdBwd`` is one FP8 linear layer, forward and backward, with
+  per-tensor delayed scaling: quantise X, W (E4M3) and dY (E5M2) row- and
+  column-wise with the fused amax, run fprop / dgrad / wgrad, then advance
+  the three histories.  On its first step a history is empty, so that step
+  uses current scaling (amax pass first).
+* ``BlockLinearFwd`` is the forward with per-block (1x128 activations,
+  128x128 weights) or MXFP8 (1x32, E8M0) scales.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import (BLOCK_1x128, BLOCK_128x128, DGRAD, E4M3, E5M2, FPROP, MX_1x32, TENSOR, WGRAD, fp8_amax,
+               fp8_amax_history_update, fp8_compute_scale, fp8_quantize, fp8_scaled_gemm)
+
+
+class ScaleState:
+    def __init__(self, fmt: int, margin: int, history_len: int = 0, device="cuda"):
+        self.fmt, self.margin = fmt, margin
+        self.amax = torch.zeros(1, dtype=torch.float32, device=device)
+        self.bias = torch.zeros(1, dtype=torch.int32, device=device)
+        self.scale = torch.ones(1, dtype=torch.float32, device=device)
+        self.scale_inv = torch.ones(1, dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.history = torch.zeros(max(history_len, 1), dtype=torch.float32, device=device) if history_len else None
+        self.pos = torch.zeros(1, dtype=torch.int64, device=device) if history_len else None
+        self.steps = 0  # host-side count of completed delayed steps
+
+    def advance(self) -> None:
+        """One delayed-scaling update: record amax, next scale from the window max, reset amax."""
+        fp8_amax_history_update(self.history, self.pos, self.amax, self.fmt, self.margin, self.bias, self.scale,
+                                self.scale_inv, self.status)
+        self.steps += 1
+
+
+def current_scaling(x: torch.Tensor, st: ScaleState) -> None:
+    """amax of x, then compute_bias -> (bias, scale, scale_inv) in st."""
+    st.amax.zero_()
+    fp8_amax(x, st.amax)
+    fp8_compute_scale(st.amax, st.fmt, st.margin, st.bias, st.scale, st.scale_inv, st.status)
+    st.amax.zero_()
+
+
+def gemm_flops(m: int, n: int, k: int) -> float:
+    return 2.0 * m * n * k
+
+
+@dataclass
+class PerTensorFwd:
+    """Per-tensor current-scaling forward: Y[M x N] fp32 = unscale(Q(X) Q(W)^T)."""
+    X: torch.Tensor
+    W: torch.Tensor
+    margin: int = 0
+
+    def __post_init__(self):
+        dev = self.X.device
+        M, K = self.X.shape
+        N = self.W.shape[0]
+        self.sx, self.sw = ScaleState(E4M3, self.margin, device=dev), ScaleState(E4M3, self.margin, device=dev)
+        self.qx = torch.empty(M, K, dtype=torch.uint8, device=dev)
+        self.qw = torch.empty(N, K, dtype=torch.uint8, device=dev)
+        self.Y = torch.empty(M, N, dtype=torch.float32, device=dev)
+        self.flops = gemm_flops(M, N, K)
+
+    def run(self) -> None:
+        current_scaling(self.X, self.sx)
+        current_scaling(self.W, self.sw)
+        fp8_quantize(self.X, E4M3, TENSOR, scale=self.sx.scale, q_row=self.qx)
+        fp8_quantize(self.W, E4M3, TENSOR, scale=self.sw.scale, q_row=self.qw)
+        fp8_scaled_gemm(FPROP, self.qx, E4M3, TENSOR, self.sx.scale_inv, self.qw, E4M3, TENSOR, self.sw.scale_inv,
+                        self.Y)
+
+
+class LinearFwdBwd:
+    """FP8 linear layer forward + backward with per-tensor delayed scaling.
+
+    X [M x K] and W [N x K] in E4M3, dY [M x N] in E5M2 (margin `grad_margin`).
+    Y  [M x N] bf16 = unscale(QX_row . QW_row^T)            (fprop)
+    dX [M x K] bf16 = unscale(QdY_row . QW_col^T)           (dgrad)
+    dW [N x K] fp32 = unscale(QdY_col . QX_col^T)           (wgrad)
+    """
+
+    def __init__(self, X: torch.Tensor, W: torch.Tensor, dY: torch.Tensor, history_len: int, margin: int = 0,
+                 grad_margin: int = 0, dw_dtype=torch.float32):
+        dev = X.device
+        M, K = X.shape
+        N = W.shape[0]
+        assert W.shape[1] == K and dY.shape == (M, N)
+        self.X, self.W, self.dY = X, W, dY
+        self.sx = ScaleState(E4M3, margin, history_len, dev)
+        self.sw = ScaleState(E4M3, margin, history_len, dev)
+        self.sg = ScaleState(E5M2, grad_margin, history_len, dev)
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.qx_row, self.qx_col = torch.empty(M, K, **u8), torch.empty(K, M, **u8)
+        self.qw_row, self.qw_col = torch.empty(N, K, **u8), torch.empty(K, N, **u8)
+        self.qg_row, self.qg_col = torch.empty(M, N, **u8), torch.empty(N, M, **u8)
+        self.Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        self.dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        self.dW = torch.empty(N, K, dtype=dw_dtype, device=dev)
+        self.flops = 3 * gemm_flops(M, N, K)
+        self.quant_bytes = 4 * (M * K + N * K + M * N)  # 2 B read + 1 B row + 1 B col per element
+
+    def quantize(self) -> None:
+        for x, st, qr, qc in ((self.X, self.sx, self.qx_row, self.qx_col), (self.W, self.sw, self.qw_row, self.qw_col),
+                              (self.dY, self.sg, self.qg_row, self.qg_col)):
+            if st.steps == 0:
+                current_scaling(x, st)  # empty history: this step scales from its own amax
+            fp8_quantize(x, st.fmt, TENSOR, scale=st.scale, q_row=qr, q_col=qc, amax=st.amax)
+
+    def gemms(self) -> None:
+        fp8_scaled_gemm(FPROP, self.qx_row, E4M3, TENSOR, self.sx.scale_inv, self.qw_row, E4M3, TENSOR,
+                        self.sw.scale_inv, self.Y)
+        fp8_scaled_gemm(DGRAD, self.qg_row, E5M2, TENSOR, self.sg.scale_inv, self.qw_col, E4M3, TENSOR,
+                        self.sw.scale_inv, self.dX)
+        fp8_scaled_gemm(WGRAD, self.qg_col, E5M2, TENSOR, self.sg.scale_inv, self.qx_col, E4M3, TENSOR,
+                        self.sx.scale_inv, self.dW)
+
+    def advance(self) -> None:
+        for st in (self.sx, self.sw, self.sg):
+            st.advance()
+
+    def run(self) -> None:
+        self.quantize()
+        self.gemms()
+        self.advance()
+
+
+class BlockLinearFwd:
+    """Forward with block scales: per-block (X 1x128, W 128x128, fp32 scales) or MXFP8 (1x32, E8M0).
+
+    Y [M x N] bf16 = sum_k (QX sx)(QW sw).  With `col=True` the column-wise (transposed) copies and
+    their scales are produced too, as the backward pass would need them."""
+
+    def __init__(self, X: torch.Tensor, W: torch.Tensor, mx: bool, col: bool = False, margin: int = 0):
+        dev = X.device
+        M, K = X.shape
+        N = W.shape[0]
+        self.X, self.W, self.mx, self.col, self.margin = X, W, mx, col, margin
+        self.gx = MX_1x32 if mx else BLOCK_1x128
+        self.gw = MX_1x32 if mx else BLOCK_128x128
+        u8 = dict(dtype=torch.uint8, device=dev)
+        sdt = dict(dtype=torch.uint8 if mx else torch.float32, device=dev)
+        cd = lambda a, b: (a + b - 1) // b
+        self.qx_row, self.qw_row = torch.empty(M, K, **u8), torch.empty(N, K, **u8)
+        if mx:
+            self.sx_row, self.sw_row = torch.empty(M, cd(K, 32), **sdt), torch.empty(N, cd(K, 32), **sdt)
+        else:
+            self.sx_row, self.sw_row = torch.empty(M, cd(K, 128), **sdt), torch.empty(cd(N, 128), cd(K, 128), **sdt)
+        if col:
+            self.qx_col, self.qw_col = torch.empty(K, M, **u8), torch.empty(K, N, **u8)
+            if mx:
+                self.sx_col, self.sw_col = torch.empty(K, cd(M, 32), **sdt), torch.empty(K, cd(N, 32), **sdt)
+            else:
+                self.sx_col = torch.empty(K, cd(M, 128), **sdt)
+                self.sw_col = torch.empty(cd(K, 128), cd(N, 128), **sdt)
+        else:
+            self.qx_col = self.qw_col = self.sx_col = self.sw_col = None
+        self.Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.flops = gemm_flops(M, N, K)
+        ncopies = 2 if col else 1
+        sbytes = lambda rows, cols, g: _scale_bytes(rows, cols, g)
+        self.quant_bytes = 2 * (M * K + N * K) + ncopies * (M * K + N * K) + sbytes(M, K, self.gx) + \
+            sbytes(N, K, self.gw) + (sbytes(K, M, self.gx) + sbytes(K, N, self.gw) if col else 0)
+
+    def quantize(self) -> None:
+        fp8_quantize(self.X, E4M3, self.gx, self.margin, q_row=self.qx_row, q_col=self.qx_col, sf_row=self.sx_row,
+                     sf_col=self.sx_col)
+        fp8_quantize(self.W, E4M3, self.gw, self.margin, q_row=self.qw_row, q_col=self.qw_col, sf_row=self.sw_row,
+                     sf_col=self.sw_col)
+
+    def gemm(self) -> None:
+        fp8_scaled_gemm(FPROP, self.qx_row, E4M3, self.gx, self.sx_row, self.qw_row, E4M3, self.gw, self.sw_row,
+                        self.Y, status=self.status)
+
+    def run(self) -> None:
+        self.quantize()
+        self.gemm()
+
+
+def _scale_bytes(rows: int, cols: int, gran: int) -> int:
+    cd = lambda a, b: (a + b - 1) // b
+    if gran == MX_1x32:
+        return rows * cd(cols, 32)
+    if gran == BLOCK_1x128:
+        return 4 * rows * cd(cols, 128)
+    if gran == BLOCK_128x128:
+        return 4 * cd(rows, 128) * cd(cols, 128)
+    return 0

@@ -1,0 +1,115 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+entry point declared in include/fp8q.h, and rejects bad arguments on the host
+before anything touches CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8q.h")
+
+FAKE = 1 << 20  # a non-NULL, 16-byte-aligned pointer value that is never dereferenced
+
+
+@pytest.fixture(scope="module")
+def L():
+    from scaling_quantization_gemm_gb300 import build as b
+    b.build()
+    import scaling_quantization_gemm_gb300 as q
+    return q.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls():
+    syms = declared_symbols()
+    for s in ["fp8_amax", "fp8_compute_scale", "fp8_amax_history_update", "fp8_quantize", "fp8_scaled_gemm"]:
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(L):
+    for s in declared_symbols():
+        assert hasattr(L, s), s
+    import scaling_quantization_gemm_gb300 as q
+    assert set(q.ENTRY_POINTS) <= set(declared_symbols())
+
+
+def test_library_exports_nothing_else(L):
+    # the shared object is built with hidden visibility: only the C ABI is exported
+    out = os.popen(f"nm -D --defined-only {L._name}").read()
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert {s for s in exported if s.startswith("fp8_")} == set(declared_symbols())
+
+
+def test_status_strings(L):
+    import scaling_quantization_gemm_gb300 as q
+    assert [q.status_name(i) for i in range(5)] == ["FP8_OK", "FP8_ERR_INVALID_ARG", "FP8_ERR_UNSUPPORTED",
+                                                    "FP8_ERR_CUDA", "FP8_ERR_TIMEOUT"]
+
+
+def _detail(L):
+    return L.fp8_last_error_detail().decode()
+
+
+def test_amax_validation(L):
+    assert L.fp8_amax(None, 4, 8, 8, FAKE, None) == 1
+    assert L.fp8_amax(FAKE, -1, 8, 8, FAKE, None) == 1
+    assert L.fp8_amax(FAKE, 4, 8, 4, FAKE, None) == 1  # ld < cols
+    assert L.fp8_amax(FAKE, 4, 8, 8, None, None) == 1
+    assert L.fp8_amax(FAKE, 4, 12, 12, FAKE, None) == 2  # cols % 8
+    assert L.fp8_amax(FAKE + 2, 4, 8, 8, FAKE, None) == 2  # misaligned
+    assert "aligned" in _detail(L)
+    assert L.fp8_amax(FAKE, 0, 8, 8, FAKE, None) == 0  # empty: valid no-op
+
+
+def test_compute_scale_and_history_validation(L):
+    assert L.fp8_compute_scale(None, 0, 0, FAKE, FAKE, FAKE, None, None) == 1
+    assert L.fp8_compute_scale(FAKE, 7, 0, FAKE, FAKE, FAKE, None, None) == 1
+    assert L.fp8_compute_scale(FAKE, 0, 0, None, None, None, None, None) == 1
+    h = [FAKE] * 3
+    assert L.fp8_amax_history_update(FAKE, 0, FAKE, FAKE, 0, 0, *h, None, None) == 1
+    assert L.fp8_amax_history_update(FAKE, 70000, FAKE, FAKE, 0, 0, *h, None, None) == 1
+    assert L.fp8_amax_history_update(FAKE, 16, None, FAKE, 0, 0, *h, None, None) == 1
+    assert L.fp8_amax_history_update(FAKE, 16, FAKE + 4, FAKE, 0, 0, *h, None, None) == 1
+
+
+def test_quantize_validation(L):
+    q = L.fp8_quantize
+    # per-tensor needs scale, takes no block scales
+    assert q(FAKE, 32, 32, 32, 0, 0, 0, None, FAKE, None, None, None, None, None) == 1
+    assert q(FAKE, 32, 32, 32, 0, 0, 0, FAKE, FAKE, None, FAKE, None, None, None) == 1
+    # no outputs
+    assert q(FAKE, 32, 32, 32, 0, 0, 0, FAKE, None, None, None, None, None, None) == 1
+    # block: needs matching scale tensors, no per-tensor scale
+    assert q(FAKE, 32, 32, 32, 0, 3, 0, None, FAKE, None, None, None, None, None) == 1
+    assert q(FAKE, 32, 32, 32, 0, 3, 0, FAKE, FAKE, None, FAKE, None, None, None) == 1
+    assert q(FAKE, 32, 32, 32, 0, 1, 0, None, FAKE, FAKE, FAKE, None, None, None) == 1  # q_col without sf_col
+    # bad enums
+    assert q(FAKE, 32, 32, 32, 2, 0, 0, FAKE, FAKE, None, None, None, None, None) == 1
+    assert q(FAKE, 32, 32, 32, 0, 9, 0, FAKE, FAKE, None, None, None, None, None) == 1
+    # column-wise output needs rows % 16 == 0
+    assert q(FAKE, 24, 32, 32, 0, 0, 0, FAKE, None, FAKE, None, None, None, None) == 2
+    # empty is a no-op
+    assert q(FAKE, 0, 32, 32, 0, 0, 0, FAKE, FAKE, None, None, None, None, None) == 0
+
+
+def test_gemm_validation(L):
+    g = L.fp8_scaled_gemm
+    args = lambda **kw: [kw.get("op", 0), kw.get("M", 128), kw.get("N", 256), kw.get("K", 128), FAKE,
+                         kw.get("lda", 128), 0, kw.get("ga", 0), FAKE, FAKE, kw.get("ldb", 128), 0, kw.get("gb", 0),
+                         FAKE, FAKE, kw.get("out", 0), kw.get("ldd", 256), None, None]
+    assert g(*args(op=5)) == 1
+    assert g(*args(M=-1)) == 1
+    assert g(*args(ga=0, gb=3)) == 1  # per-tensor on one side only
+    assert g(*args(ldd=128)) == 1
+    assert g(*args(K=120, lda=128, ldb=128)) == 2  # K % 16
+    assert g(*args(N=200, ldd=256)) == 2  # N % 16
+    assert g(*args(ga=3, gb=3, K=160, lda=160, ldb=160)) == 2  # block-scaled needs K % 128
+    assert g(*args(lda=64)) == 1  # lda < K
+    assert g(*args(M=0)) == 0  # empty output: no-op
