@@ -385,6 +385,56 @@ def run_reference(args, rank, world):
     }), flush=True)
 
 
+# ------------------------------------------------------- profiling cases
+
+def run_case(name: str, launches: int = 3) -> None:
+    """One kernel on inputs larger than L2 but a few hundred MB in total, `launches` times (for ncu)."""
+    import torch
+
+    import scaling_quantization_gemm_gb300 as q
+    torch.cuda.set_device(0)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    kind, shape = PROFILE_CASES[name]
+    if kind.startswith("gemm"):
+        M, N, K = shape
+        A = torch.randint(0, 0x7E, (M, K), dtype=torch.uint8, device="cuda", generator=g)
+        B = torch.randint(0, 0x7E, (N, K), dtype=torch.uint8, device="cuda", generator=g)
+        D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        if kind == "gemm_tensor":
+            sa = sb = torch.ones(1, device="cuda")
+            ga = gb = q.TENSOR
+        else:
+            sa = torch.randint(120, 135, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
+            sb = torch.randint(120, 135, (N, K // 32), dtype=torch.uint8, device="cuda", generator=g)
+            ga = gb = q.MX_1x32
+        for _ in range(launches):
+            q.fp8_scaled_gemm(q.FPROP, A, 0, ga, sa, B, 0, gb, sb, D)
+    else:
+        R, C = shape
+        x = torch.randn(R, C, device="cuda", generator=g).to(torch.bfloat16)
+        qr = torch.empty(R, C, dtype=torch.uint8, device="cuda")
+        qc = torch.empty(C, R, dtype=torch.uint8, device="cuda")
+        amax = torch.zeros(1, device="cuda")
+        sr = torch.empty(R, C // 32, dtype=torch.uint8, device="cuda")
+        sc = torch.empty(C, R // 32, dtype=torch.uint8, device="cuda")
+        one = torch.ones(1, device="cuda")
+        for _ in range(launches):
+            if kind == "quant_tensor":
+                q.fp8_quantize(x, 0, q.TENSOR, scale=one, q_row=qr, q_col=qc, amax=amax)
+            else:
+                q.fp8_quantize(x, 0, q.MX_1x32, q_row=qr, q_col=qc, sf_row=sr, sf_col=sc)
+    torch.cuda.synchronize()
+    print(f"case {name} ok")
+
+
+PROFILE_CASES = {
+    "gemm_tensor": ("gemm_tensor", (16384, 8192, 8192)),
+    "gemm_mx": ("gemm_mx", (16384, 8192, 8192)),
+    "quant_tensor": ("quant_tensor", (16384, 8192)),
+    "quant_mx": ("quant_mx", (16384, 8192)),
+}
+
+
 # -------------------------------------------------------------- plumbing
 
 def barrier(world):
@@ -398,7 +448,8 @@ def max_over_ranks(x: float, world: int) -> float:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -412,6 +463,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--reference-rows", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=sorted(PROFILE_CASES), default=None,
+                    help="run one kernel on a small (> L2) case for an ncu capture, then exit")
     args = ap.parse_args(argv)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -426,6 +479,9 @@ def main(argv=None):
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
             dist.init_process_group("nccl")
+    if args.case:
+        run_case(args.case)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:
