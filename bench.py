@@ -403,6 +403,11 @@ def run_case(name: str, launches: int = 3) -> None:
         if kind == "gemm_tensor":
             sa = sb = torch.ones(1, device="cuda")
             ga = gb = q.TENSOR
+        elif kind == "gemm_block":
+            e = torch.randint(-4, 5, (M, K // 128), device="cuda", generator=g).float()
+            sa = torch.exp2(e)
+            sb = torch.exp2(torch.randint(-4, 5, ((N + 127) // 128, K // 128), device="cuda", generator=g).float())
+            ga, gb = q.BLOCK_1x128, q.BLOCK_128x128
         else:
             sa = torch.randint(120, 135, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
             sb = torch.randint(120, 135, (N, K // 32), dtype=torch.uint8, device="cuda", generator=g)
@@ -430,6 +435,7 @@ def run_case(name: str, launches: int = 3) -> None:
 PROFILE_CASES = {
     "gemm_tensor": ("gemm_tensor", (16384, 8192, 8192)),
     "gemm_mx": ("gemm_mx", (16384, 8192, 8192)),
+    "gemm_block": ("gemm_block", (8192, 11008, 4096)),
     "quant_tensor": ("quant_tensor", (16384, 8192)),
     "quant_mx": ("quant_mx", (16384, 8192)),
 }

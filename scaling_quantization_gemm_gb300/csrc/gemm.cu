@@ -7,22 +7,28 @@
 // Effective FP8 Training", "Key Questions Answered").
 //
 // Design (one persistent CTA per SM, warp-specialised):
-//   warp 0      TMA producer: 128x128-byte A tiles and 256x128-byte B tiles,
+//   warp 0      TMA producer: 128x128-byte A tiles and BNx128-byte B tiles,
 //               128-byte swizzle, into a 4-stage shared-memory ring.
 //   warp 1      allocates TMEM and issues tcgen05.mma (one thread); each
 //               128-wide K tile is four K=32 MMAs.
 //   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), unscale, convert,
 //               store.  Each warp owns the 32 TMEM lanes (= tile rows) that
 //               its warp index selects.
-//   warps 6-9   (block-scaled kernel only) scale-factor writers: per K tile
-//               they load the E8M0 (or power-of-two fp32) scales of the
-//               tile's rows and store them into TMEM next to the accumulator.
-// Per-tensor: two 128x256 fp32 accumulators in TMEM (512 columns), so the
-// epilogue of one tile overlaps the main loop of the next; the unscale
-// 2^-(ea+eb) is applied in the epilogue.  Block-scaled: the scales enter the
-// MMA itself (kind::mxf8f6f4 with block_scale); one accumulator + scale
-// columns.  Power-of-two fp32 block scales (1x128, 128x128) are re-encoded as
-// E8M0 exactly and repeated over the four 32-wide K sub-blocks they cover.
+//   warps 6-9   (block-scaled kernel only) scale-factor writers.
+// Two fp32 accumulators live in TMEM so the epilogue of one tile overlaps the
+// main loop of the next.
+// Per-tensor: 128x256 tiles (2 x 256 TMEM columns); the unscale
+// 2^-(ea+eb) is applied in the epilogue.
+// Block-scaled: the scales enter the MMA itself (kind::mxf8f6f4 with
+// block_scale, E8M0 scale per 32 K).  Tiles are 128x224 so that two
+// accumulators (448 columns) and a 16-column scale slot per pipeline stage
+// (64 columns) fit the 512 TMEM columns.  Power-of-two fp32 block scales
+// (1x128, 128x128) are re-encoded as E8M0 exactly and repeated over the four
+// 32-wide K sub-blocks they cover.  The scale writers load the scales of four
+// K tiles per 16-byte vector, one group ahead of use, and store into TMEM the
+// cells the MMA reads: the scale of A row m at lane m, column m/32; the scale
+// of B row n at lane 32q + n%32, column n/32, in every lane quarter q (each
+// quarter of the tensor core reads its own copy); byte = K sub-block.
 //
 // Every barrier wait is bounded (2 s); a wait that gives up raises a shared
 // abort flag, every role leaves its loop, in-flight TMA loads and MMAs are
@@ -46,17 +52,14 @@ constexpr int kABytes = BM * BK;
 constexpr int kBBytes = BN * BK;
 constexpr int kGroupM = 16;  // tile raster: groups of 16 M-tiles walk N together (L2 reuse)
 
-// TMEM layout of the block-scaled kernel.
-constexpr int kSfColBase = 256;   // scale factors start after the 256 accumulator columns
-constexpr int kSfColsPerStage = 16;  // 8 for A (4 used), 8 for B
+// Block-scaled kernel: tile width, TMEM layout.
+constexpr int BN_BS = 224;
+constexpr int kBBytesBS = BN_BS * BK;
+constexpr int kSfColBase = 2 * BN_BS;  // scale slots start after the two accumulators (448)
+constexpr int kSfColsPerStage = 16;    // A scales at +0 (4 columns), B scales at +8 (7 columns)
+constexpr int kSfbCols = BN_BS / 32;
 
-// Scale-factor placement in TMEM for kind::mxf8f6f4, scale_vec::1X, M = 128:
-// the scale of operand row r for the four 32-wide K sub-blocks of one K tile is
-// one 32-bit word (byte i = sub-block i, selected by the MMA's scale-factor id)
-// at lane 32*q + (r % 32) for every lane quarter q, column (r / 32) of the
-// operand's scale region.
-constexpr int kSfaCols = 4;  // 128 rows of A
-constexpr int kSfbCols = 8;  // 256 rows of B
+enum { SF_MX = 0, SF_ROW = 1, SF_BLOCK = 2 };  // E8M0 1x32 | fp32 per row (1x128) | fp32 per 128 rows (128x128)
 
 struct GemmArgs {
     int M, N, K;
@@ -67,8 +70,8 @@ struct GemmArgs {
     const float* sb;
     const void* sfa;  // block scales
     const void* sfb;
-    int ga, gb;
-    int64_t sfa_ld, sfb_ld;  // row pitch of the scale tensors, in elements
+    int64_t sfa_ld, sfb_ld;  // row pitch of the scale tensors in elements (bytes for E8M0, floats for fp32)
+    int vec_a, vec_b;        // scale rows allow 16-byte loads of four K tiles
     int32_t* status;
 };
 
@@ -132,8 +135,9 @@ __device__ void drain_mma(uint64_t* bar) {
 
 // ------------------------------------------------------------------ producer
 
+template <int BN_>
 __device__ __forceinline__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmArgs& g,
-                                              uint8_t (*sa)[kABytes], uint8_t (*sb)[kBBytes], uint64_t* full,
+                                              uint8_t (*sa)[kABytes], uint8_t (*sb)[BN_ * BK], uint64_t* full,
                                               uint64_t* empty, volatile int* abort_flag) {
     int stage = 0;
     uint32_t phase = 0;
@@ -148,9 +152,9 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tmA, const CUte
                 ok = false;
                 break;
             }
-            mbar_arrive_expect_tx(smem_u32(&full[stage]), kABytes + kBBytes);
+            mbar_arrive_expect_tx(smem_u32(&full[stage]), kABytes + BN_ * BK);
             tma_load_2d(smem_u32(sa[stage]), tmA, smem_u32(&full[stage]), kt * BK, tm * BM);
-            tma_load_2d(smem_u32(sb[stage]), tmB, smem_u32(&full[stage]), kt * BK, tn * BN);
+            tma_load_2d(smem_u32(sb[stage]), tmB, smem_u32(&full[stage]), kt * BK, tn * BN_);
             last_phase[stage] = phase;
             used[stage] = true;
             if (++stage == kStages) {
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem = S.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) producer_loop(&tmA, &tmB, g, S.a, S.b, S.full, S.empty, abort_flag);
+        if (lane == 0) producer_loop<BN>(&tmA, &tmB, g, S.a, S.b, S.full, S.empty, abort_flag);
     } else if (warp == 1) {
         if (lane == 0) {
             int stage = 0, acc = 0;
@@ -280,8 +284,8 @@ __global__ void __launch_bounds__(192, 1)
 
 struct alignas(1024) SmemBS {
     uint8_t a[kStages][kABytes];
-    uint8_t b[kStages][kBBytes];
-    uint64_t full[kStages], empty[kStages], tfull, tempty, drain;
+    uint8_t b[kStages][kBBytesBS];
+    uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], drain;
     uint32_t tmem_base;
     int abort_flag;
     int bad_scale;
@@ -296,17 +300,47 @@ __device__ __forceinline__ uint32_t e8m0_of_pow2(float f, bool& bad) {
     return ex;
 }
 
-// The 32-bit scale word (four K sub-blocks of 32) of operand row `row` for K tile `kt`.
-__device__ __forceinline__ uint32_t scale_word(const void* sf, int gran, int64_t ld, int64_t row, int64_t rows, int kt,
-                                               bool& bad) {
-    if (row >= rows) return 0x7F7F7F7Fu;  // rows past the edge hold zeros: any finite scale
-    if (gran == FP8_SCALE_MX_1x32) return __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(sf) + row * ld) + kt);
-    const float* f = static_cast<const float*>(sf);
-    const float v = (gran == FP8_SCALE_BLOCK_1x128) ? __ldg(f + row * ld + kt) : __ldg(f + (row >> 7) * ld + kt);
-    return e8m0_of_pow2(v, bad) * 0x01010101u;
+template <int KIND>
+__device__ __forceinline__ uint32_t sf_neutral() {
+    return KIND == SF_MX ? 0x7F7F7F7Fu : 0x3F800000u;  // scale 1.0 (rows past the edge hold zeros)
 }
 
-template <int OUT_BF16>
+// Raw scale data of operand row `row` for the four K tiles kt0 .. kt0+3: E8M0
+// words (four bytes = four 32-wide K sub-blocks each) or fp32 bit patterns.
+template <int KIND>
+__device__ __forceinline__ uint4 sf_load_group(const void* sf, int64_t ld, int64_t row, int64_t rows, int kt0,
+                                               int k_tiles, bool vec) {
+    const uint32_t z = sf_neutral<KIND>();
+    uint4 r = make_uint4(z, z, z, z);
+    if (row >= rows) return r;
+    const uint32_t* p;
+    if constexpr (KIND == SF_MX)
+        p = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(sf) + row * ld) + kt0;
+    else
+        p = reinterpret_cast<const uint32_t*>(static_cast<const float*>(sf) + (KIND == SF_ROW ? row : (row >> 7)) * ld) +
+            kt0;
+    if (vec && kt0 + 4 <= k_tiles) return __ldg(reinterpret_cast<const uint4*>(p));
+    r.x = __ldg(p);
+    if (kt0 + 1 < k_tiles) r.y = __ldg(p + 1);
+    if (kt0 + 2 < k_tiles) r.z = __ldg(p + 2);
+    if (kt0 + 3 < k_tiles) r.w = __ldg(p + 3);
+    return r;
+}
+
+__device__ __forceinline__ uint32_t comp(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+
+template <int KIND>
+__device__ __forceinline__ uint32_t sf_word(uint32_t raw, bool& bad) {
+    if constexpr (KIND == SF_MX) return raw;
+    return e8m0_of_pow2(__uint_as_float(raw), bad) * 0x01010101u;
+}
+
+struct SfGroup {
+    uint4 a;
+    uint4 b[kSfbCols];
+};
+
+template <int OUT_BF16, int KA, int KB>
 __global__ void __launch_bounds__(320, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             GemmArgs g, uint32_t idesc) {
@@ -320,8 +354,10 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(smem_u32(&S.full[s]), 1 + 4);  // TMA producer + four scale writers
             mbar_init(smem_u32(&S.empty[s]), 1);
         }
-        mbar_init(smem_u32(&S.tfull), 1);
-        mbar_init(smem_u32(&S.tempty), 4);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&S.tfull[a]), 1);
+            mbar_init(smem_u32(&S.tempty[a]), 4);
+        }
         mbar_init(smem_u32(&S.drain), 1);
         S.abort_flag = 0;
         S.bad_scale = 0;
@@ -339,15 +375,16 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tmem = S.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) producer_loop(&tmA, &tmB, g, S.a, S.b, S.full, S.empty, abort_flag);
+        if (lane == 0) producer_loop<BN_BS>(&tmA, &tmB, g, S.a, S.b, S.full, S.empty, abort_flag);
     } else if (warp == 1) {
         if (lane == 0) {
-            int stage = 0;
+            int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < g.num_tiles; t += gridDim.x) {
-                if (!mbar_wait_bounded(smem_u32(&S.tempty), acc_phase ^ 1, abort_flag)) break;
+                if (!mbar_wait_bounded(smem_u32(&S.tempty[acc]), acc_phase ^ 1, abort_flag)) break;
                 tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * BN_BS);
                 for (int kt = 0; kt < g.k_tiles; ++kt) {
                     if (!mbar_wait_bounded(smem_u32(&S.full[stage]), phase, abort_flag)) {
                         ok = false;
@@ -360,7 +397,7 @@ __global__ void __launch_bounds__(320, 1)
                     const uint32_t sfb_t = sfa_t + 8;
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
-                        tc_mma_mxf8f6f4(tmem, ad + 2 * k, bd + 2 * k, idesc | ((uint32_t)k << 29) | ((uint32_t)k << 4),
+                        tc_mma_mxf8f6f4(d, ad + 2 * k, bd + 2 * k, idesc | ((uint32_t)k << 29) | ((uint32_t)k << 4),
                                         sfa_t, sfb_t, (kt | k) != 0 ? 1u : 0u);
                     tc_commit(smem_u32(&S.empty[stage]));
                     if (++stage == kStages) {
@@ -369,81 +406,111 @@ __global__ void __launch_bounds__(320, 1)
                     }
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(&S.tfull));
-                acc_phase ^= 1;
+                tc_commit(smem_u32(&S.tfull[acc]));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
             }
             drain_mma(&S.drain);
         }
     } else if (warp < 6) {
         const int q = warp & 3;
+        int acc = 0;
         uint32_t acc_phase = 0;
-        const float one = 1.0f;
         for (int t = blockIdx.x; t < g.num_tiles; t += gridDim.x) {
-            bool ok = mbar_wait_bounded(smem_u32(&S.tfull), acc_phase, abort_flag);
+            bool ok = mbar_wait_bounded(smem_u32(&S.tfull[acc]), acc_phase, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             int tm, tn;
             tile_coords(t, g, tm, tn);
             const int64_t row = (int64_t)tm * BM + q * 32 + lane;
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN_BS);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < BN_BS / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
-                const int64_t col0 = (int64_t)tn * BN + c * 32;
-                if (row < g.M) store_row32<OUT_BF16>(g, row, col0, r, one, one);
+                const int64_t col0 = (int64_t)tn * BN_BS + c * 32;
+                if (row < g.M) store_row32<OUT_BF16>(g, row, col0, r, 1.0f, 1.0f);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&S.tempty));
-            acc_phase ^= 1;
+            if (lane == 0) mbar_arrive(smem_u32(&S.tempty[acc]));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
         }
     } else {
-        // Scale-factor writers: warp (6..9) writes the lanes of quarter q = warp % 4.
+        // Scale-factor writers: warp 6..9 owns TMEM lane quarter q = warp % 4.  Each quarter of the
+        // tensor core reads scales from its own 32 lanes: the A scale of its rows 32q + l (column q of
+        // the slot) and the B scales of all tile columns n (columns 8 + n/32 at lane 32q + n % 32), so
+        // every writer stores its A column and a full copy of the B columns.  Scales are loaded one
+        // group of four K tiles ahead of use.
         const int q = warp & 3;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const int groups = (g.k_tiles + 3) / 4;
         int stage = 0;
         uint32_t phase = 0;
-        bool ok = true, bad = false;
-        for (int t = blockIdx.x; ok && t < g.num_tiles; t += gridDim.x) {
+        bool bad = false;
+
+        auto load = [&](int t, int grp, SfGroup& dst) {
             int tm, tn;
             tile_coords(t, g, tm, tn);
-            const int64_t arow0 = (int64_t)tm * BM + lane, brow0 = (int64_t)tn * BN + lane;
-            for (int kt0 = 0; ok && kt0 < g.k_tiles; kt0 += 4) {
-                // Load four K tiles' worth of scale words at once (loads in flight together).
-                uint32_t wa[4][kSfaCols], wb[4][kSfbCols];
+            dst.a = sf_load_group<KA>(g.sfa, g.sfa_ld, (int64_t)tm * BM + q * 32 + lane, g.M, 4 * grp, g.k_tiles,
+                                      g.vec_a);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int kt = min(kt0 + j, g.k_tiles - 1);
+            for (int j = 0; j < kSfbCols; ++j)
+                dst.b[j] = sf_load_group<KB>(g.sfb, g.sfb_ld, (int64_t)tn * BN_BS + 32 * j + lane, g.N, 4 * grp,
+                                             g.k_tiles, g.vec_b);
+        };
+        auto emit = [&](const SfGroup& src, int grp) -> bool {
 #pragma unroll
-                    for (int c = 0; c < kSfaCols; ++c) wa[j][c] = scale_word(g.sfa, g.ga, g.sfa_ld, arow0 + 32 * c, g.M, kt, bad);
+            for (int jj = 0; jj < 4; ++jj) {
+                if (4 * grp + jj >= g.k_tiles) break;
+                bool w = mbar_wait_bounded(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag);
+                if (!__all_sync(0xffffffffu, w)) return false;
+                tc_fence_after();
+                const uint32_t slot = tmem + lane_base + (uint32_t)(kSfColBase + stage * kSfColsPerStage);
+                tmem_st_32x32b_x1(slot + q, sf_word<KA>(comp(src.a, jj), bad));
+                uint32_t wb[8];
 #pragma unroll
-                    for (int c = 0; c < kSfbCols; ++c) wb[j][c] = scale_word(g.sfb, g.gb, g.sfb_ld, brow0 + 32 * c, g.N, kt, bad);
+                for (int j = 0; j < kSfbCols; ++j) wb[j] = sf_word<KB>(comp(src.b[j], jj), bad);
+                wb[7] = 0x7F7F7F7Fu;
+                tmem_st_32x32b_x8(slot + 8, wb);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.full[stage]));
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
                 }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (kt0 + j >= g.k_tiles) break;
-                    bool w = mbar_wait_bounded(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag);
-                    w = __all_sync(0xffffffffu, w);
-                    if (!w) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t col = tmem + lane_base + (uint32_t)(kSfColBase + stage * kSfColsPerStage);
-                    tmem_st_32x32b_x4(col, wa[j][0], wa[j][1], wa[j][2], wa[j][3]);
-                    tmem_st_32x32b_x4(col + 8, wb[j][0], wb[j][1], wb[j][2], wb[j][3]);
-                    tmem_st_32x32b_x4(col + 12, wb[j][4], wb[j][5], wb[j][6], wb[j][7]);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&S.full[stage]));
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
+            }
+            return true;
+        };
+        // walk this CTA's (tile, group) pairs, loading one group ahead
+        auto advance = [&](int& t, int& grp) -> bool {
+            if (++grp == groups) {
+                grp = 0;
+                t += gridDim.x;
+            }
+            return t < g.num_tiles;
+        };
+        int t = blockIdx.x, grp = 0;
+        if (t < g.num_tiles && groups > 0) {
+            SfGroup b0, b1;
+            load(t, grp, b0);
+            while (true) {
+                int t1 = t, g1 = grp;
+                const bool has1 = advance(t1, g1);
+                if (has1) load(t1, g1, b1);
+                if (!emit(b0, grp) || !has1) break;
+                t = t1;
+                grp = g1;
+                int t2 = t, g2 = grp;
+                const bool has2 = advance(t2, g2);
+                if (has2) load(t2, g2, b0);
+                if (!emit(b1, grp) || !has2) break;
+                t = t2;
+                grp = g2;
             }
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&S.bad_scale, 1);
@@ -502,36 +569,68 @@ fp8_status prepare_kernel(const void* func, size_t smem) {
     return FP8_OK;
 }
 
+int sf_kind(int gran) { return gran == FP8_SCALE_MX_1x32 ? SF_MX : gran == FP8_SCALE_BLOCK_1x128 ? SF_ROW : SF_BLOCK; }
+
+template <int OUT_BF16, int KA, int KB>
+fp8_status launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g, uint32_t idesc, int grid,
+                     cudaStream_t st) {
+    const size_t smem = sizeof(SmemBS) + 1024;
+    auto k = gemm_blockscaled_kernel<OUT_BF16, KA, KB>;
+    fp8_status s = prepare_kernel(reinterpret_cast<const void*>(k), smem);
+    if (s != FP8_OK) return s;
+    k<<<grid, 320, smem, st>>>(tmA, tmB, g, idesc);
+    return check_launch("gemm_blockscaled_kernel launch");
+}
+
+template <int OUT_BF16>
+fp8_status dispatch_bs(int ka, int kb, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
+                       uint32_t idesc, int grid, cudaStream_t st) {
+#define FP8Q_BS(A, B) \
+    if (ka == A && kb == B) return launch_bs<OUT_BF16, A, B>(tmA, tmB, g, idesc, grid, st);
+    FP8Q_BS(SF_MX, SF_MX)
+    FP8Q_BS(SF_ROW, SF_BLOCK)
+    FP8Q_BS(SF_ROW, SF_ROW)
+    FP8Q_BS(SF_BLOCK, SF_BLOCK)
+    FP8Q_BS(SF_BLOCK, SF_ROW)
+    FP8Q_BS(SF_MX, SF_ROW)
+    FP8Q_BS(SF_MX, SF_BLOCK)
+    FP8Q_BS(SF_ROW, SF_MX)
+    FP8Q_BS(SF_BLOCK, SF_MX)
+#undef FP8Q_BS
+    return FP8_ERR_UNSUPPORTED;
+}
+
 }  // namespace
 
 fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, int fa, int ga, const void* sfa,
                        const uint8_t* B, int64_t ldb, int fb, int gb, const void* sfb, void* D, int out_bf16,
                        int64_t ldd, int32_t* status, cudaStream_t st) {
+    const bool blockscaled = ga != FP8_SCALE_TENSOR;
+    const int bn = blockscaled ? BN_BS : BN;
     GemmArgs g;
     g.M = (int)M;
     g.N = (int)N;
     g.K = (int)K;
     g.tiles_m = (int)((M + BM - 1) / BM);
-    g.tiles_n = (int)((N + BN - 1) / BN);
+    g.tiles_n = (int)((N + bn - 1) / bn);
     g.k_tiles = (int)((K + BK - 1) / BK);
     g.num_tiles = g.tiles_m * g.tiles_n;
     g.D = D;
     g.ldd = ldd;
     g.status = status;
-    g.ga = ga;
-    g.gb = gb;
     g.sa = g.sb = nullptr;
     g.sfa = g.sfb = nullptr;
     g.sfa_ld = g.sfb_ld = 0;
+    g.vec_a = g.vec_b = 0;
 
     CUtensorMap tmA, tmB;
     fp8_status s = make_operand_map(&tmA, A, M, K, lda, BM);
     if (s != FP8_OK) return s;
-    s = make_operand_map(&tmB, B, N, K, ldb, BN);
+    s = make_operand_map(&tmB, B, N, K, ldb, bn);
     if (s != FP8_OK) return s;
 
     const int grid = std::min(g.num_tiles, device_sm_count());
-    if (ga == FP8_SCALE_TENSOR) {
+    if (!blockscaled) {
         g.sa = static_cast<const float*>(sfa);
         g.sb = static_cast<const float*>(sfb);
         const uint32_t idesc = idesc_f8f6f4(fa, fb, BM, BN);
@@ -548,19 +647,18 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
     g.sfa = sfa;
     g.sfb = sfb;
     const int64_t KT = (K + BK - 1) / BK;
-    // row pitch of each scale tensor: MX in bytes-as-u32-words is handled by the word index (kt)
+    // row pitch of each scale tensor: E8M0 rows are K/32 bytes, fp32 rows are ceil(K/128) floats
     g.sfa_ld = (ga == FP8_SCALE_MX_1x32) ? K / 32 : KT;
     g.sfb_ld = (gb == FP8_SCALE_MX_1x32) ? K / 32 : KT;
-    const uint32_t idesc = idesc_mxf8f6f4(fa, fb, BM, BN, 0, 0);
-    const size_t smem = sizeof(SmemBS) + 1024;
-    if (out_bf16) {
-        if ((s = prepare_kernel(reinterpret_cast<const void*>(gemm_blockscaled_kernel<1>), smem)) != FP8_OK) return s;
-        gemm_blockscaled_kernel<1><<<grid, 320, smem, st>>>(tmA, tmB, g, idesc);
-    } else {
-        if ((s = prepare_kernel(reinterpret_cast<const void*>(gemm_blockscaled_kernel<0>), smem)) != FP8_OK) return s;
-        gemm_blockscaled_kernel<0><<<grid, 320, smem, st>>>(tmA, tmB, g, idesc);
-    }
-    return check_launch("gemm_blockscaled_kernel launch");
+    auto vec_ok = [](const void* p, int gran, int64_t ld) {
+        const int64_t row_bytes = gran == FP8_SCALE_MX_1x32 ? ld : 4 * ld;
+        return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && row_bytes % 16 == 0;
+    };
+    g.vec_a = vec_ok(sfa, ga, g.sfa_ld);
+    g.vec_b = vec_ok(sfb, gb, g.sfb_ld);
+    const uint32_t idesc = idesc_mxf8f6f4(fa, fb, BM, BN_BS, 0, 0);
+    return out_bf16 ? dispatch_bs<1>(sf_kind(ga), sf_kind(gb), tmA, tmB, g, idesc, grid, st)
+                    : dispatch_bs<0>(sf_kind(ga), sf_kind(gb), tmA, tmB, g, idesc, grid, st);
 }
 
 }  // namespace fp8q

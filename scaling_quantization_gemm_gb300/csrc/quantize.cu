@@ -8,11 +8,15 @@
 // per-block / MXFP8 scales ("Per-Tensor and Per-Block Scaling Strategies for
 // Effective FP8 Training", "Key Questions Answered").
 //
-// All of it is HBM-bound.  The cast kernel reads each bf16 element once with
-// 16-byte coalesced loads, computes block maxima in registers (warp shuffles),
-// writes the row-wise codes straight from registers, and stages the tile in
-// shared memory to produce the transposed column-wise codes, so one read feeds
-// both outputs.  Amax is reduced per warp, per CTA, then one atomic per CTA.
+// All of it is HBM-bound.  The cast kernel streams 128x128 bf16 tiles through
+// a three-deep TMA ring in shared memory (loads for the next two tiles are in
+// flight while one is processed), computes block maxima in registers (warp
+// shuffles), writes the row-wise codes, and reads the same tile down its
+// columns for the transposed column-wise codes, so one HBM read feeds both
+// outputs.  The fused amax is reduced per warp, per CTA, then one atomic per
+// CTA.
+#include <cudaTypedefs.h>
+
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -23,13 +27,12 @@ namespace fp8q {
 
 namespace {
 
-constexpr int kTile = 128;          // tile is kTile x kTile bf16 elements
+constexpr int kTile = 128;     // tile is kTile x kTile bf16 elements (32 KB)
 constexpr int kThreads = 256;
-constexpr int kPitch = kTile + 8;   // smem row pitch in bf16 (272 bytes: conflict-free column reads)
+constexpr int kQStages = 2;    // TMA ring depth (3 CTAs per SM: up to 6 tiles in flight per SM)
 
 struct QuantArgs {
-    const uint16_t* x;
-    int64_t rows, cols, ld;
+    int64_t rows, cols;
     int margin;
     const float* scale;
     uint8_t* q_row;
@@ -39,32 +42,103 @@ struct QuantArgs {
     float* amax;
     int64_t tiles_c, ntiles;
     int do_row, do_col;
+    int32_t* status;
+};
+
+struct alignas(1024) QuantSmem {
+    uint16_t tile[kQStages][kTile * kTile];
+    uint64_t full[kQStages];
+    uint64_t empty[kQStages];  // one arrival per warp when it is done with the stage
+    uint32_t red[2][8];
+    uint32_t col_part[4][64];
+    uint32_t am[8];
+    int abort_flag;
 };
 
 __device__ __forceinline__ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-template <int FMT>
-__device__ __forceinline__ uint2 encode8(const uint4& v, float s) {
-    uint32_t c0 = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s));
-    uint32_t c1 = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.y), s), __fmul_rn(bf16_hi(v.y), s));
-    uint32_t c2 = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s));
-    uint32_t c3 = cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(v.w), s), __fmul_rn(bf16_hi(v.w), s));
-    return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+// Bias of a block from the bf16 bit pattern m of its amax (|x| bits): for a
+// normal finite m the exponent and the top mantissa bits are read directly
+// (m > 1.75 <=> the 7 fraction bits exceed 0x60); other m take the general path.
+__device__ __forceinline__ int bias_bf16(uint32_t m, int fmt, int margin) {
+    if (m - 0x80u < 0x7F00u) {
+        const int ef = fmt == FP8_E4M3 ? 8 : 15;
+        int e = ef + 127 - (int)(m >> 7) - ((m & 0x7Fu) > 0x60u ? 1 : 0) - margin;
+        return min(max(e, -126), 127);
+    }
+    bool nf = false;
+    return bias_from_amax(bf16bits_to_float(m), fmt, margin, &nf);
 }
 
-// Encode the low (HALF = 0) or high (HALF = 1) bf16 of 32 words (32 rows of one
-// column) into 32 codes packed in 8 words, row order.
+// Running |x| maximum of bf16 pairs: one instruction per word.  max.xorsign.abs
+// keeps the larger magnitude (its sign bit is meaningless and masked off at the
+// end); .NaN makes a NaN win, so a NaN input yields a NaN amax.
+__device__ __forceinline__ uint32_t absmax_acc(uint32_t acc, uint32_t w) {
+    uint32_t r;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(w));
+    return r;
+}
+__device__ __forceinline__ uint32_t absmax_fold(uint32_t acc) { return fold2(acc & 0x7FFF7FFFu); }
+
+// 2^e as a bf16x2 pair, e in [-126, 127].
+__device__ __forceinline__ uint32_t pow2_bf16x2(int e) {
+    const uint32_t b = (uint32_t)(e + 127) << 7;
+    return b | (b << 16);
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Scaled cast of the two bf16 in word w: x * 2^e is exact in bf16 whenever it
+// is a normal number, and when it is not its magnitude is below 2^-126 and
+// encodes to a signed zero either way, so the codes equal those of the fp32
+// product.  Low byte = low element.
+template <int FMT>
+__device__ __forceinline__ uint32_t encode2(uint32_t w, uint32_t s2) {
+    const uint32_t p = mul_bf16x2(w, s2);
+    return cvt_fp8x2<FMT>(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 encode8(const uint4& v, uint32_t s2) {
+    return make_uint2(encode2<FMT>(v.x, s2) | (encode2<FMT>(v.y, s2) << 16),
+                      encode2<FMT>(v.z, s2) | (encode2<FMT>(v.w, s2) << 16));
+}
+
+// Same with an arbitrary fp32 scale (per-tensor scales that are not powers of two).
+template <int FMT>
+__device__ __forceinline__ uint32_t encode2_f32(uint32_t w, float s) {
+    return cvt_fp8x2<FMT>(__fmul_rn(bf16_lo(w), s), __fmul_rn(bf16_hi(w), s));
+}
+template <int FMT>
+__device__ __forceinline__ uint2 encode8_f32(const uint4& v, float s) {
+    return make_uint2(encode2_f32<FMT>(v.x, s) | (encode2_f32<FMT>(v.y, s) << 16),
+                      encode2_f32<FMT>(v.z, s) | (encode2_f32<FMT>(v.w, s) << 16));
+}
+
+// Column-wise: the low (HALF = 0) or high (HALF = 1) bf16 of 32 words (32 rows
+// of one column) -> 32 codes in 8 words, row order.
 template <int FMT, int HALF>
-__device__ __forceinline__ void encode_column32(const uint32_t (&w)[32], float s, uint32_t (&o)[8]) {
+__device__ __forceinline__ void encode_column32(const uint32_t (&w)[32], uint32_t s2, uint32_t (&o)[8]) {
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        float a0 = HALF ? bf16_hi(w[4 * p + 0]) : bf16_lo(w[4 * p + 0]);
-        float a1 = HALF ? bf16_hi(w[4 * p + 1]) : bf16_lo(w[4 * p + 1]);
-        float a2 = HALF ? bf16_hi(w[4 * p + 2]) : bf16_lo(w[4 * p + 2]);
-        float a3 = HALF ? bf16_hi(w[4 * p + 3]) : bf16_lo(w[4 * p + 3]);
-        uint32_t lo = cvt_fp8x2<FMT>(__fmul_rn(a0, s), __fmul_rn(a1, s));
-        uint32_t hi = cvt_fp8x2<FMT>(__fmul_rn(a2, s), __fmul_rn(a3, s));
-        o[p] = lo | (hi << 16);
+    for (int p = 0; p < 16; ++p) {
+        // rows 2p, 2p+1 of this column as one bf16x2 word
+        const uint32_t pair = HALF ? __byte_perm(w[2 * p], w[2 * p + 1], 0x7632) : __byte_perm(w[2 * p], w[2 * p + 1], 0x5410);
+        const uint32_t c = encode2<FMT>(pair, s2);
+        if (p & 1) o[p >> 1] |= c << 16; else o[p >> 1] = c;
+    }
+}
+
+template <int FMT, int HALF>
+__device__ __forceinline__ void encode_column32_f32(const uint32_t (&w)[32], float s, uint32_t (&o)[8]) {
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+        const uint32_t pair = HALF ? __byte_perm(w[2 * p], w[2 * p + 1], 0x7632) : __byte_perm(w[2 * p], w[2 * p + 1], 0x5410);
+        const uint32_t c = encode2_f32<FMT>(pair, s);
+        if (p & 1) o[p >> 1] |= c << 16; else o[p >> 1] = c;
     }
 }
 
@@ -75,56 +149,103 @@ __device__ __forceinline__ void store_col32(uint8_t* q_col, int64_t c, int64_t r
     if (row0 + 16 < rows) *reinterpret_cast<uint4*>(dst + 16) = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// One CTA walks 128x128 tiles (grid-stride).  Thread t loads the 16-byte chunk
-// column j = t % 16 of rows t/16 + 16 i, i = 0..7.
+// Persistent CTAs walk 128x128 tiles (grid-stride).  Thread 0 keeps the next
+// tile's TMA load in flight; each warp releases a stage on its own (an mbarrier
+// arrival), so warps never wait for one another except where a tile needs a
+// cross-warp reduction (128x128 blocks, 128x1 column blocks).  Row pass: thread t holds the 16-byte chunk column j = t % 16 of
+// rows t/16 + 16 i, i = 0..7.  Column pass: warp w covers column pairs
+// lane + 32 (w & 1) over the 32-row segment w / 2.
 template <int GRAN, int FMT>
-__global__ void __launch_bounds__(kThreads) quantize_tile_kernel(QuantArgs a) {
-    __shared__ __align__(16) uint16_t sx[kTile * kPitch];
-    __shared__ uint32_t red[2][8];
-    __shared__ uint32_t col_part[4][64];
-
+__global__ void __launch_bounds__(kThreads, 3) quantize_tile_kernel(const __grid_constant__ CUtensorMap tmX, QuantArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    QuantSmem& S = *reinterpret_cast<QuantSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int j = tid & 15;
     const int rsub = tid >> 4;
+    const int64_t n_my = (a.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
 
+    // tiles that need a block-wide reduction keep the CTA in lock step
+    const bool lockstep = GRAN == FP8_SCALE_BLOCK_128x128 || (GRAN == FP8_SCALE_BLOCK_1x128 && a.do_col);
+    if (tid == 0) {
+        for (int s = 0; s < kQStages; ++s) {
+            mbar_init(smem_u32(&S.full[s]), 1);
+            mbar_init(smem_u32(&S.empty[s]), kThreads / 32);
+        }
+        S.abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    auto issue = [&](int64_t i) {  // TMA load of this CTA's i-th tile into stage i % kQStages
+        const int64_t tile = blockIdx.x + i * gridDim.x;
+        const int st = (int)(i % kQStages);
+        mbar_arrive_expect_tx(smem_u32(&S.full[st]), kTile * kTile * 2);
+        tma_load_2d(smem_u32(S.tile[st]), &tmX, smem_u32(&S.full[st]), (int)((tile % a.tiles_c) * kTile),
+                    (int)((tile / a.tiles_c) * kTile));
+    };
+    int64_t issued = 0;  // meaningful in thread 0
+    if (tid == 0) {
+        tma_prefetch_desc(&tmX);
+        for (; issued < kQStages && issued < n_my; ++issued) issue(issued);
+    }
+
+    uint32_t s2_tensor = 0;
     float s_tensor = 1.0f;
-    if constexpr (GRAN == FP8_SCALE_TENSOR) s_tensor = *a.scale;
-
+    bool pow2_tensor = true;
+    if constexpr (GRAN == FP8_SCALE_TENSOR) {
+        // a positive normal power of two 2^e is exact as a bf16x2 pair; any other scale takes the fp32 path
+        s_tensor = *a.scale;
+        const uint32_t u = __float_as_uint(s_tensor);
+        pow2_tensor = (u & 0x807FFFFFu) == 0 && (u >> 23) - 1u < 254u;
+        const uint32_t sb = u >> 16;
+        s2_tensor = sb | (sb << 16);
+    }
     uint32_t amax_acc = 0;
-    int parity = 0;
 
-    for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, parity ^= 1) {
+    for (int64_t i = 0; i < n_my; ++i) {
+        if (tid == 0 && i >= 1 && i + 1 < n_my) {
+            // stage (i+1) % 2 held tile i-1: wait until every warp has released it, then refill
+            const int64_t u = i - 1;
+            if (mbar_wait_bounded(smem_u32(&S.empty[u % kQStages]), (uint32_t)((u / kQStages) & 1), &S.abort_flag)) {
+                issue(i + 1);
+                issued = i + 2;
+            }
+        }
+        const int st = (int)(i % kQStages);
+        bool ok = mbar_wait_bounded(smem_u32(&S.full[st]), (uint32_t)((i / kQStages) & 1), &S.abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (lockstep) {
+            if (__syncthreads_or(!ok)) break;
+        } else if (!ok) {
+            break;
+        }
+        const uint16_t* T = S.tile[st];
+        const int64_t tile = blockIdx.x + i * gridDim.x;
         const int64_t r0 = (tile / a.tiles_c) * kTile, c0 = (tile % a.tiles_c) * kTile;
         const int64_t col = c0 + 8 * j;
         const bool col_ok = col < a.cols;
+        const int parity = (int)(i & 1);
 
         uint4 v[8];
+        uint32_t cm[8];  // |x| max of each chunk, bf16 bits
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int64_t r = r0 + rsub + 16 * i;
-            v[i] = (col_ok && r < a.rows) ? ld_stream_v4(a.x + r * a.ld + col) : make_uint4(0, 0, 0, 0);
-        }
-        uint32_t cm[8];  // |x| max of each loaded chunk, bf16 bits
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            cm[i] = fold2(absmax2(absmax2(absmax2(absmax2(0u, v[i].x), v[i].y), v[i].z), v[i].w));
-            amax_acc = max(amax_acc, cm[i]);
+        for (int k = 0; k < 8; ++k) {
+            v[k] = *reinterpret_cast<const uint4*>(&T[(rsub + 16 * k) * kTile + 8 * j]);
+            cm[k] = absmax_fold(absmax_acc(absmax_acc(absmax_acc(v[k].x, v[k].y), v[k].z), v[k].w));
+            amax_acc = max(amax_acc, cm[k]);
         }
 
-        // 128x128 blocks: one exponent for the whole tile, shared by both outputs.
         int e_tile = 0;
         if constexpr (GRAN == FP8_SCALE_BLOCK_128x128) {
             uint32_t m = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) m = max(m, cm[i]);
+            for (int k = 0; k < 8; ++k) m = max(m, cm[k]);
             m = __reduce_max_sync(0xffffffffu, m);
-            if (lane == 0) red[parity][warp] = m;
+            if (lane == 0) S.red[parity][warp] = m;
             __syncthreads();
-            m = red[parity][0];
+            m = S.red[parity][0];
 #pragma unroll
-            for (int w = 1; w < 8; ++w) m = max(m, red[parity][w]);
-            bool nf = false;
-            e_tile = bias_from_amax(bf16bits_to_float(m), FMT, a.margin, &nf);
+            for (int w = 1; w < 8; ++w) m = max(m, S.red[parity][w]);
+            e_tile = bias_bf16(m, FMT, a.margin);
             if (tid == 0) {
                 const int64_t tr = r0 / kTile, tc = c0 / kTile;
                 if (a.do_row) static_cast<float*>(a.sf_row)[tr * cdiv(a.cols, kTile) + tc] = pow2_exact(-e_tile);
@@ -135,66 +256,68 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_kernel(QuantArgs a) {
         // ---------------------------------------------------------- row-wise
         if (a.do_row) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int64_t r = r0 + rsub + 16 * i;
-                const bool ok = col_ok && r < a.rows;
-                float s;
+            for (int k = 0; k < 8; ++k) {
+                const int64_t r = r0 + rsub + 16 * k;
+                const bool okr = col_ok && r < a.rows;
+                uint32_t s2;
                 if constexpr (GRAN == FP8_SCALE_TENSOR) {
-                    s = s_tensor;
+                    s2 = s2_tensor;
                 } else if constexpr (GRAN == FP8_SCALE_BLOCK_128x128) {
-                    s = pow2_exact(e_tile);
+                    s2 = pow2_bf16x2(e_tile);
                 } else if constexpr (GRAN == FP8_SCALE_MX_1x32) {
-                    uint32_t m = cm[i];
+                    uint32_t m = cm[k];
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                    bool nf = false;
-                    const int e = bias_from_amax(bf16bits_to_float(m), FMT, a.margin, &nf);
-                    s = pow2_exact(e);
-                    if ((j & 3) == 0 && ok)
+                    const int e = bias_bf16(m, FMT, a.margin);
+                    s2 = pow2_bf16x2(e);
+                    if ((j & 3) == 0 && okr)
                         static_cast<uint8_t*>(a.sf_row)[r * cdiv(a.cols, 32) + (col >> 5)] = (uint8_t)(127 - e);
                 } else {  // 1x128
-                    uint32_t m = cm[i];
+                    uint32_t m = cm[k];
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                    bool nf = false;
-                    const int e = bias_from_amax(bf16bits_to_float(m), FMT, a.margin, &nf);
-                    s = pow2_exact(e);
+                    const int e = bias_bf16(m, FMT, a.margin);
+                    s2 = pow2_bf16x2(e);
                     if (j == 0 && r < a.rows)
                         static_cast<float*>(a.sf_row)[r * cdiv(a.cols, kTile) + c0 / kTile] = pow2_exact(-e);
                 }
-                if (ok) *reinterpret_cast<uint2*>(a.q_row + r * a.cols + col) = encode8<FMT>(v[i], s);
+                if (okr) {
+                    uint2 c;
+                    if (GRAN != FP8_SCALE_TENSOR || pow2_tensor)
+                        c = encode8<FMT>(v[k], s2);
+                    else
+                        c = encode8_f32<FMT>(v[k], s_tensor);
+                    *reinterpret_cast<uint2*>(a.q_row + r * a.cols + col) = c;
+                }
             }
         }
 
         // ------------------------------------------------------- column-wise
         if (a.do_col) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(&sx[(rsub + 16 * i) * kPitch + 8 * j]) = v[i];
-            __syncthreads();
             const int cp = lane + 32 * (warp & 1);  // column pair within the tile
             const int seg = warp >> 1;              // 32-row segment within the tile
             uint32_t w[32];
 #pragma unroll
-            for (int r = 0; r < 32; ++r) w[r] = *reinterpret_cast<const uint32_t*>(&sx[(32 * seg + r) * kPitch + 2 * cp]);
-            uint32_t mm = 0;
+            for (int r = 0; r < 32; ++r) w[r] = *reinterpret_cast<const uint32_t*>(&T[(32 * seg + r) * kTile + 2 * cp]);
+            uint32_t mm = w[0];
 #pragma unroll
-            for (int r = 0; r < 32; ++r) mm = absmax2(mm, w[r]);
+            for (int r = 1; r < 32; ++r) mm = absmax_acc(mm, w[r]);
+            mm &= 0x7FFF7FFFu;
 
-            float sA, sB;
+            uint32_t sA, sB;
             const int64_t ca = c0 + 2 * cp, cb = ca + 1;
             const int64_t row0 = r0 + 32 * seg;
             if constexpr (GRAN == FP8_SCALE_TENSOR) {
-                sA = sB = s_tensor;
+                sA = sB = s2_tensor;
             } else if constexpr (GRAN == FP8_SCALE_BLOCK_128x128) {
-                sA = sB = pow2_exact(e_tile);
+                sA = sB = pow2_bf16x2(e_tile);
             } else if constexpr (GRAN == FP8_SCALE_MX_1x32) {
-                bool nf = false;
-                const int eA = bias_from_amax(bf16bits_to_float(mm & 0xFFFFu), FMT, a.margin, &nf);
-                const int eB = bias_from_amax(bf16bits_to_float(mm >> 16), FMT, a.margin, &nf);
-                sA = pow2_exact(eA);
-                sB = pow2_exact(eB);
+                const int eA = bias_bf16(mm & 0xFFFFu, FMT, a.margin);
+                const int eB = bias_bf16(mm >> 16, FMT, a.margin);
+                sA = pow2_bf16x2(eA);
+                sB = pow2_bf16x2(eB);
                 if (row0 < a.rows) {
                     uint8_t* sf = static_cast<uint8_t*>(a.sf_col);
                     const int64_t nb = cdiv(a.rows, 32);
@@ -202,14 +325,14 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_kernel(QuantArgs a) {
                     if (cb < a.cols) sf[cb * nb + (row0 >> 5)] = (uint8_t)(127 - eB);
                 }
             } else {  // 1x128 -> 128x1 column blocks: combine the four 32-row segments
-                col_part[seg][cp] = mm;
+                S.col_part[seg][cp] = mm;
                 __syncthreads();
-                uint32_t m4 = __vmaxu2(__vmaxu2(col_part[0][cp], col_part[1][cp]), __vmaxu2(col_part[2][cp], col_part[3][cp]));
-                bool nf = false;
-                const int eA = bias_from_amax(bf16bits_to_float(m4 & 0xFFFFu), FMT, a.margin, &nf);
-                const int eB = bias_from_amax(bf16bits_to_float(m4 >> 16), FMT, a.margin, &nf);
-                sA = pow2_exact(eA);
-                sB = pow2_exact(eB);
+                const uint32_t m4 = __vmaxu2(__vmaxu2(S.col_part[0][cp], S.col_part[1][cp]),
+                                             __vmaxu2(S.col_part[2][cp], S.col_part[3][cp]));
+                const int eA = bias_bf16(m4 & 0xFFFFu, FMT, a.margin);
+                const int eB = bias_bf16(m4 >> 16, FMT, a.margin);
+                sA = pow2_bf16x2(eA);
+                sB = pow2_bf16x2(eB);
                 if (seg == 0) {
                     float* sf = static_cast<float*>(a.sf_col);
                     const int64_t nb = cdiv(a.rows, kTile);
@@ -218,29 +341,53 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_kernel(QuantArgs a) {
                 }
             }
             uint32_t o[8];
-            if (ca < a.cols) {
-                encode_column32<FMT, 0>(w, sA, o);
-                store_col32(a.q_col, ca, a.rows, row0, o);
+            if (GRAN == FP8_SCALE_TENSOR && !pow2_tensor) {
+                if (ca < a.cols) {
+                    encode_column32_f32<FMT, 0>(w, s_tensor, o);
+                    store_col32(a.q_col, ca, a.rows, row0, o);
+                }
+                if (cb < a.cols) {
+                    encode_column32_f32<FMT, 1>(w, s_tensor, o);
+                    store_col32(a.q_col, cb, a.rows, row0, o);
+                }
+            } else {
+                if (ca < a.cols) {
+                    encode_column32<FMT, 0>(w, sA, o);
+                    store_col32(a.q_col, ca, a.rows, row0, o);
+                }
+                if (cb < a.cols) {
+                    encode_column32<FMT, 1>(w, sB, o);
+                    store_col32(a.q_col, cb, a.rows, row0, o);
+                }
             }
-            if (cb < a.cols) {
-                encode_column32<FMT, 1>(w, sB, o);
-                store_col32(a.q_col, cb, a.rows, row0, o);
-            }
-            __syncthreads();  // sx / col_part are rewritten by the next tile
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&S.empty[st]));  // this warp is done with the stage
     }
 
+    __syncthreads();
+    if (S.abort_flag) {
+        // giving up: let the loads already issued land before the CTA exits
+        if (tid == 0) {
+            for (int64_t i = issued > kQStages ? issued - kQStages : 0; i < issued; ++i) {
+                const int st = (int)(i % kQStages);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(smem_u32(&S.full[st]), (uint32_t)((i / kQStages) & 1)))
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+            }
+            if (a.status) atomicOr(a.status, FP8_STATUS_TIMEOUT);
+        }
+        return;
+    }
     if (a.amax) {
-        uint32_t m = __reduce_max_sync(0xffffffffu, amax_acc);
-        __shared__ uint32_t am[8];
-        __syncthreads();
-        if (lane == 0) am[warp] = m;
+        const uint32_t m = __reduce_max_sync(0xffffffffu, amax_acc);
+        if (lane == 0) S.am[warp] = m;
         __syncthreads();
         if (tid == 0) {
+            uint32_t mx = S.am[0];
 #pragma unroll
-            for (int w = 1; w < 8; ++w) m = max(m, am[w]);
-            m = max(m, am[0]);
-            atomicMax(reinterpret_cast<unsigned int*>(a.amax), m << 16);
+            for (int w = 1; w < 8; ++w) mx = max(mx, S.am[w]);
+            atomicMax(reinterpret_cast<unsigned int*>(a.amax), mx << 16);
         }
     }
 }
@@ -320,21 +467,44 @@ __global__ void __launch_bounds__(1024) history_kernel(float* hist, int len, int
     }
 }
 
-template <int GRAN, int FMT>
-int quant_grid(int64_t ntiles) {
-    static int occ = [] {
-        int o = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, quantize_tile_kernel<GRAN, FMT>, kThreads, 0);
-        return o > 0 ? o : 1;
+PFN_cuTensorMapEncodeTiled_v12000 q_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     }();
-    const int64_t cap = (int64_t)device_sm_count() * occ;
-    return (int)(ntiles < cap ? ntiles : cap);
+    return fn;
 }
 
 template <int GRAN, int FMT>
-fp8_status launch_quant(const QuantArgs& a, cudaStream_t st) {
-    const int grid = quant_grid<GRAN, FMT>(a.ntiles);
-    quantize_tile_kernel<GRAN, FMT><<<grid, kThreads, 0, st>>>(a);
+fp8_status launch_quant(const CUtensorMap& tm, const QuantArgs& a, cudaStream_t st) {
+    auto k = quantize_tile_kernel<GRAN, FMT>;
+    const size_t smem = sizeof(QuantSmem) + 1024;
+    static std::mutex mu;
+    static int occ_dev[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int occ;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || occ_dev[dev] == 0) {
+            cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            int o = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k, kThreads, smem);
+            occ = o > 0 ? o : 1;
+            if (dev >= 0 && dev < 64) occ_dev[dev] = occ;
+        } else {
+            occ = occ_dev[dev];
+        }
+    }
+    const int64_t cap = (int64_t)device_sm_count() * occ;
+    const int grid = (int)(a.ntiles < cap ? a.ntiles : cap);
+    k<<<grid, kThreads, smem, st>>>(tm, a);
     return check_launch("quantize kernel launch");
 }
 
@@ -380,11 +550,20 @@ fp8_status launch_history(float* hist, int len, int64_t* pos, float* amax, int f
 fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int gran, int margin,
                            const float* scale, uint8_t* q_row, uint8_t* q_col, void* sf_row, void* sf_col,
                            float* amax, cudaStream_t st) {
+    auto fn = q_encode_fn();
+    FP8_REQUIRE(fn != nullptr, FP8_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    CUtensorMap tm;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kTile, (cuuint32_t)kTile};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    FP8_REQUIRE(r == CUDA_SUCCESS, FP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     QuantArgs a;
-    a.x = static_cast<const uint16_t*>(x);
     a.rows = rows;
     a.cols = cols;
-    a.ld = ld;
     a.margin = margin;
     a.scale = scale;
     a.q_row = q_row;
@@ -396,9 +575,10 @@ fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld
     a.ntiles = ((rows + kTile - 1) / kTile) * a.tiles_c;
     a.do_row = q_row != nullptr;
     a.do_col = q_col != nullptr;
+    a.status = nullptr;
 #define FP8Q_QDISPATCH(G)                                                         \
     case G:                                                                       \
-        return fmt == FP8_E4M3 ? launch_quant<G, FP8_E4M3>(a, st) : launch_quant<G, FP8_E5M2>(a, st);
+        return fmt == FP8_E4M3 ? launch_quant<G, FP8_E4M3>(tm, a, st) : launch_quant<G, FP8_E5M2>(tm, a, st);
     switch (gran) {
         FP8Q_QDISPATCH(FP8_SCALE_TENSOR)
         FP8Q_QDISPATCH(FP8_SCALE_BLOCK_1x128)

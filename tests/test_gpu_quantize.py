@@ -226,3 +226,14 @@ def test_quantize_empty_is_noop(q):
     x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
     out = torch.empty(0, 64, dtype=torch.uint8, device="cuda")
     q.fp8_quantize(x, 0, q.TENSOR, scale=torch.ones(1, device="cuda"), q_row=out)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("scale_val", [0.3, 3.7, -2.0, 1e-30, 2.0 ** -130])
+def test_quantize_tensor_arbitrary_scale(q, fmt, scale_val):
+    """A per-tensor scale that is not a positive normal power of two takes the fp32 multiply path."""
+    x = wl.random_bf16(55 + fmt, 144, 264, "wide", 1.0)
+    qr, _, qc, _, _ = _run_gpu_quant(q, x, fmt, 0, 0, True, True, scale_val=float(np.float32(scale_val)))
+    rr, rc = oracle.quantize_tensor(x, fmt, np.float32(scale_val), row=True, col=True)
+    assert_codes_equal(qr, rr, fmt, "row")
+    assert_codes_equal(qc, rc, fmt, "col")
