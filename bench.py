@@ -436,6 +436,7 @@ PROFILE_CASES = {
     "gemm_tensor": ("gemm_tensor", (16384, 8192, 8192)),
     "gemm_mx": ("gemm_mx", (16384, 8192, 8192)),
     "gemm_block": ("gemm_block", (8192, 11008, 4096)),
+    "gemm_ffn_fprop": ("gemm_tensor", (16384, 20480, 5120)),
     "quant_tensor": ("quant_tensor", (16384, 8192)),
     "quant_mx": ("quant_mx", (16384, 8192)),
 }

@@ -280,6 +280,166 @@ __global__ void __launch_bounds__(192, 1)
     if (threadIdx.x == 0 && S.abort_flag && g.status) atomicOr(g.status, FP8_STATUS_TIMEOUT);
 }
 
+// ======================================================= per-tensor GEMM, CTA pair
+
+// Two CTAs on two SMs compute one 256x256 tile with tcgen05.mma.cta_group::2:
+// each CTA holds 128 rows of A and 128 rows of B per K tile (32 KB per stage,
+// 6 stages) and 128 rows of the accumulator in its own TMEM.  The even CTA of
+// the pair issues the MMAs for both.  Both producers signal the even CTA's
+// `full` barrier; the MMA commits arrive on the `empty` / `tfull` barriers of
+// both CTAs; both epilogues release an accumulator on the even CTA's `tempty`.
+constexpr int kPairStages = 6;
+constexpr int kPairRows = 128;                      // rows of A and of B per CTA per tile
+constexpr int kPairTile = 2 * kPairRows;            // 256 x 256 output tile per pair
+constexpr int kPairHalfBytes = kPairRows * BK;      // 16 KB
+constexpr int kPairStageBytes = 2 * kPairHalfBytes; // A half + B half, per CTA
+
+struct alignas(1024) SmemPair {
+    uint8_t a[kPairStages][kPairHalfBytes];
+    uint8_t b[kPairStages][kPairHalfBytes];
+    uint64_t full[kPairStages], empty[kPairStages], tfull[2], tempty[2], drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+template <int OUT_BF16>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tensor_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g,
+                            uint32_t idesc) {
+    extern __shared__ uint8_t smem_raw[];
+    SmemPair& S = *reinterpret_cast<SmemPair*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs of the pair
+    const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    volatile int* abort_flag = &S.abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(smem_u32(&S.full[s]), 2);   // one expect_tx arrival from each producer of the pair
+            mbar_init(smem_u32(&S.empty[s]), 1);  // the MMA commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&S.tfull[a]), 1);
+            mbar_init(smem_u32(&S.tempty[a]), 8);  // four epilogue warps in each CTA
+        }
+        mbar_init(smem_u32(&S.drain), 1);
+        S.abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&S.tmem_base), 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = cid; ok && t < g.num_tiles; t += ncl) {
+                int tm, tn;
+                tile_coords(t, g, tm, tn);
+                for (int kt = 0; kt < g.k_tiles; ++kt) {
+                    if (!mbar_wait_bounded(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_leader = map_to_cta(smem_u32(&S.full[stage]), 0);
+                    mbar_arrive_expect_tx_cluster(full_leader, kPairStageBytes);
+                    tma_load_2d_pair(smem_u32(S.a[stage]), &tmA, full_leader, kt * BK, tm * kPairTile + (int)rank * kPairRows);
+                    tma_load_2d_pair(smem_u32(S.b[stage]), &tmB, full_leader, kt * BK, tn * kPairTile + (int)rank * kPairRows);
+                    if (++stage == kPairStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {  // giving up: the loads signal the other CTA's barrier, so just let them land
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 2000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = cid; ok && t < g.num_tiles; t += ncl) {
+                if (!mbar_wait_bounded(smem_u32(&S.tempty[acc]), acc_phase ^ 1, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                for (int kt = 0; kt < g.k_tiles; ++kt) {
+                    if (!mbar_wait_bounded(smem_u32(&S.full[stage]), phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_kmajor_sw128(smem_u32(S.a[stage]));
+                    const uint64_t bd = sdesc_kmajor_sw128(smem_u32(S.b[stage]));
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        tc_mma_f8f6f4_pair(d, ad + 2 * k, bd + 2 * k, idesc, (kt | k) != 0 ? 1u : 0u);
+                    tc_commit_pair_multicast(smem_u32(&S.empty[stage]), 0x3);
+                    if (++stage == kPairStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair_multicast(smem_u32(&S.tfull[acc]), 0x3);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            tc_commit_pair(smem_u32(&S.drain));
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&S.drain), 0))
+                if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+    } else {
+        const int q = warp & 3;
+        const float sa = *g.sa, sb = *g.sb;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = cid; t < g.num_tiles; t += ncl) {
+            bool ok = mbar_wait_bounded(smem_u32(&S.tfull[acc]), acc_phase, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            int tm, tn;
+            tile_coords(t, g, tm, tn);
+            const int64_t row = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows + q * 32 + lane;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
+                const int64_t col0 = (int64_t)tn * kPairTile + c * 32;
+                if (row < g.M) store_row32<OUT_BF16>(g, row, col0, r, sa, sb);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&S.tempty[acc]), 0));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // neither CTA leaves while the other may still signal its barriers
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
+    if (threadIdx.x == 0 && S.abort_flag && g.status) atomicOr(g.status, FP8_STATUS_TIMEOUT);
+}
+
 // ========================================================= block-scaled GEMM
 
 struct alignas(1024) SmemBS {
@@ -569,6 +729,52 @@ fp8_status prepare_kernel(const void* func, size_t smem) {
     return FP8_OK;
 }
 
+template <int OUT_BF16>
+fp8_status launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g, uint32_t idesc,
+                       cudaStream_t st) {
+    auto k = gemm_tensor_pair_kernel<OUT_BF16>;
+    const size_t smem = sizeof(SmemPair) + 1024;
+    fp8_status s = prepare_kernel(reinterpret_cast<const void*>(k), smem);
+    if (s != FP8_OK) return s;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // one resident pair per two SMs (as many as fit), never more pairs than tiles
+    static std::mutex mu;
+    static int max_clusters[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int mc;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || max_clusters[dev] == 0) {
+            cfg.gridDim = dim3(2 * (device_sm_count() / 2));
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k), &cfg) != cudaSuccess || n <= 0) {
+                cudaGetLastError();
+                n = device_sm_count() / 2;
+            }
+            mc = n;
+            if (dev >= 0 && dev < 64) max_clusters[dev] = n;
+        } else {
+            mc = max_clusters[dev];
+        }
+    }
+    const int pairs = std::max(1, std::min(g.num_tiles, mc));
+    cfg.gridDim = dim3(2 * pairs);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, tmA, tmB, g, idesc);
+    FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "gemm_tensor_pair_kernel launch: %s", cudaGetErrorString(e));
+    return check_launch("gemm_tensor_pair_kernel launch");
+}
+
 int sf_kind(int gran) { return gran == FP8_SCALE_MX_1x32 ? SF_MX : gran == FP8_SCALE_BLOCK_1x128 ? SF_ROW : SF_BLOCK; }
 
 template <int OUT_BF16, int KA, int KB>
@@ -606,12 +812,14 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
                        const uint8_t* B, int64_t ldb, int fb, int gb, const void* sfb, void* D, int out_bf16,
                        int64_t ldd, int32_t* status, cudaStream_t st) {
     const bool blockscaled = ga != FP8_SCALE_TENSOR;
+    const bool pair = !blockscaled && M > BM;  // two-SM tiles once the second half of a 256-row tile has work
     const int bn = blockscaled ? BN_BS : BN;
     GemmArgs g;
     g.M = (int)M;
     g.N = (int)N;
     g.K = (int)K;
-    g.tiles_m = (int)((M + BM - 1) / BM);
+    const int bm = pair ? kPairTile : BM;
+    g.tiles_m = (int)((M + bm - 1) / bm);
     g.tiles_n = (int)((N + bn - 1) / bn);
     g.k_tiles = (int)((K + BK - 1) / BK);
     g.num_tiles = g.tiles_m * g.tiles_n;
@@ -626,8 +834,14 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
     CUtensorMap tmA, tmB;
     fp8_status s = make_operand_map(&tmA, A, M, K, lda, BM);
     if (s != FP8_OK) return s;
-    s = make_operand_map(&tmB, B, N, K, ldb, bn);
+    s = make_operand_map(&tmB, B, N, K, ldb, pair ? kPairRows : bn);
     if (s != FP8_OK) return s;
+    if (pair) {
+        g.sa = static_cast<const float*>(sfa);
+        g.sb = static_cast<const float*>(sfb);
+        const uint32_t idesc = idesc_f8f6f4(fa, fb, kPairTile, BN);
+        return out_bf16 ? launch_pair<1>(tmA, tmB, g, idesc, st) : launch_pair<0>(tmA, tmB, g, idesc, st);
+    }
 
     const int grid = std::min(g.num_tiles, device_sm_count());
     if (!blockscaled) {
