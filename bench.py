@@ -222,7 +222,7 @@ def run_ours(args, rank, world):
     quant_ms = sum(per_op[n] for n, _, k, *_ in ops if k == "quant")
     quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9
     value = step_flops * world / (ms_step * 1e-3) / 1e12
-    traffic = load_traffic("gemm_tensor_kernel")
+    traffic = load_traffic("gemm_tensor_pair_kernel")
     peak_note = f"{'sustained' if long_loop else 'burst'} bf16 x {FP8_OVER_BF16:g} (nominal fp8/bf16), {pk_src}"
 
     cpu = cpu_baseline(host) if (rank == 0 and not args.no_cpu_baseline) else None
@@ -233,7 +233,7 @@ def run_ours(args, rank, world):
         "config": {"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (about 2 GB read per step), no flush",
                    "step_gemm_tflop": round(step_flops / 1e12, 3), "input_gen_s": round(gen_s, 1)},
-        "roofline": {"bound": "tensor", "kernel": "gemm_tensor_kernel (13B FFN fprop/dgrad/wgrad)",
+        "roofline": {"bound": "tensor", "kernel": "gemm_tensor_pair_kernel (13B FFN fprop/dgrad/wgrad)",
                      "achieved": round(tensor_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(tensor_tflops / fp8_peak, 4), "peak_source": peak_note,
                      "traffic": traffic},
@@ -284,21 +284,21 @@ def run_e2e(args, d, host, ops, stream, c1, c5, c4, c3, step_flops, world):
 
 
 def load_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if one matches the current source."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch of `kernel` at the benchmark shape, from the committed ncu summary
+    (profiles/traffic.txt), or None when the kernel source has changed since it was captured."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    with open(p) as f:
-        d = json.load(f)
-    e = d.get(kernel)
-    if not e:
-        return None
-    src = os.path.join(ROOT, "scaling_quantization_gemm_gb300", "csrc", e.get("source", ""))
-    if e.get("source_sha1") and os.path.exists(src):
-        import hashlib
-        if hashlib.sha1(open(src, "rb").read()).hexdigest() != e["source_sha1"]:
+    for line in open(p):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("kernel") != kernel:
+            continue
+        src = os.path.join(ROOT, "scaling_quantization_gemm_gb300", "csrc", f.get("source", ""))
+        if not os.path.exists(src) or hashlib.sha1(open(src, "rb").read()).hexdigest() != f.get("source_sha1"):
             return None
-    return e.get("bytes_per_launch")
+        return int(f["bytes_per_launch"])
+    return None
 
 
 # ------------------------------------------------------------- CPU oracle
