@@ -38,6 +38,7 @@
 #include <algorithm>
 #include <mutex>
 #include <set>
+#include <map>
 #include <utility>
 
 #include "common.cuh"
@@ -72,6 +73,7 @@ struct GemmArgs {
     const void* sfb;
     int64_t sfa_ld, sfb_ld;  // row pitch of the scale tensors in elements (bytes for E8M0, floats for fp32)
     int vec_a, vec_b;        // scale rows allow 16-byte loads of four K tiles
+    int pair;                // CTA-pair kernel (256-row tiles)
     int32_t* status;
 };
 
@@ -451,13 +453,14 @@ struct alignas(1024) SmemBS {
     int bad_scale;
 };
 
-// fp32 power of two in [2^-127, 2^127] -> E8M0 code (its biased exponent).
-__device__ __forceinline__ uint32_t e8m0_of_pow2(float f, bool& bad) {
+// fp32 power of two in [2^-127, 2^127] -> E8M0 code (its biased exponent), branch-free.  Any other
+// value ORs a non-zero bit into `bad` (a register, not a flag in memory).
+__device__ __forceinline__ uint32_t e8m0_of_pow2(float f, uint32_t& bad) {
     const uint32_t u = __float_as_uint(f);
-    if (u == 0x00400000u) return 0;  // 2^-127 is the only subnormal power of two in range
     const uint32_t ex = (u >> 23) & 0xFFu;
-    if ((u & 0x807FFFFFu) != 0 || ex == 0 || ex == 255) bad = true;
-    return ex;
+    const uint32_t sub = (u == 0x00400000u);  // 2^-127, the only subnormal power of two in range
+    bad |= (1u - sub) & (uint32_t)(((u & 0x807FFFFFu) != 0) | (ex == 0) | (ex == 255));
+    return sub ? 0u : ex;
 }
 
 template <int KIND>
@@ -490,7 +493,7 @@ __device__ __forceinline__ uint4 sf_load_group(const void* sf, int64_t ld, int64
 __device__ __forceinline__ uint32_t comp(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
 
 template <int KIND>
-__device__ __forceinline__ uint32_t sf_word(uint32_t raw, bool& bad) {
+__device__ __forceinline__ uint32_t sf_word(uint32_t raw, uint32_t& bad) {
     if constexpr (KIND == SF_MX) return raw;
     return e8m0_of_pow2(__uint_as_float(raw), bad) * 0x01010101u;
 }
@@ -609,7 +612,7 @@ __global__ void __launch_bounds__(320, 1)
         const int groups = (g.k_tiles + 3) / 4;
         int stage = 0;
         uint32_t phase = 0;
-        bool bad = false;
+        uint32_t bad = 0;
 
         auto load = [&](int t, int grp, SfGroup& dst) {
             int tm, tn;
@@ -673,13 +676,305 @@ __global__ void __launch_bounds__(320, 1)
                 grp = g2;
             }
         }
-        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&S.bad_scale, 1);
+        if (__any_sync(0xffffffffu, bad != 0) && lane == 0) atomicOr(&S.bad_scale, 1);
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, 512);
+    if (threadIdx.x == 0 && g.status) {
+        if (S.abort_flag) atomicOr(g.status, FP8_STATUS_TIMEOUT);
+        if (S.bad_scale) atomicOr(g.status, FP8_STATUS_BAD_BLOCK_SCALE);
+    }
+}
+
+// ================================================== block-scaled GEMM, CTA pair
+
+// A pair computes a 256x224 tile with tcgen05.mma.cta_group::2 ... block_scale:
+// each CTA holds 128 rows of A and 112 rows of B per K tile (30 KB per stage,
+// 4 stages) and 128 rows of the accumulator.  Each CTA's tensor core reads the
+// scales of its own A rows and of all 224 B rows from its own TMEM, so both
+// CTAs' scale writers fill their own scale slots (A row m: lane m, column m/32;
+// B row n: lane 32q + n%32, column 8 + n/32, every quarter q).  The producer
+// TMA-loads the scales of each group of four K tiles (16 bytes per row: the A
+// rows of this CTA and all B rows of the tile) into a four-slot shared-memory
+// ring, two groups ahead; the writers read them there.  A producer arrives on the even CTA's
+// `full` barrier only after its own CTA's scale slot for that stage is written
+// (local `sf_full` barrier), so the even CTA's MMA sees the scales of both CTAs.
+constexpr int kBsPairStages = 4;
+constexpr int kBsPairB = BN_BS / 2;                    // 112 rows of B per CTA
+constexpr int kBsPairABytes = kPairRows * BK;          // 16 KB
+constexpr int kBsPairBBytes = kBsPairB * BK;           // 14 KB
+constexpr int kBsPairStageBytes = kBsPairABytes + kBsPairBBytes;
+constexpr int kScaleSlots = 4;
+constexpr int kScaleAhead = 2;  // scale groups loaded ahead of the group being consumed
+constexpr int kScaleBlockRowsB = 3;                    // 224 B rows touch at most three 128-row blocks
+
+struct alignas(1024) SmemBsPair {
+    uint8_t a[kBsPairStages][kBsPairABytes];
+    uint8_t b[kBsPairStages][kBsPairBBytes];
+    alignas(128) uint8_t sa[kScaleSlots][kPairRows * 16];  // per row: four K tiles x 4 bytes (E8M0 x4 or one fp32)
+    alignas(128) uint8_t sb[kScaleSlots][BN_BS * 16];
+    uint64_t full[kBsPairStages], empty[kBsPairStages], sf_full[kBsPairStages], tfull[2], tempty[2], drain;
+    uint64_t scale_full[kScaleSlots], scale_empty[kScaleSlots];
+    uint32_t tmem_base;
+    int abort_flag;
+    int bad_scale;
+};
+
+// Scale-tensor TMA box of one group for an operand of kind KIND: the rows of the box and its bytes.
+template <int KIND>
+__host__ __device__ constexpr int scale_box_rows(int rows) {
+    return KIND == SF_BLOCK ? (rows == kPairRows ? 1 : kScaleBlockRowsB) : rows;
+}
+
+// Scale word (four E8M0 bytes) of local row r, K tile jj of the group, from the shared-memory slot.
+template <int KIND>
+__device__ __forceinline__ uint32_t sf_word_smem(const uint8_t* slot, int r, int jj, int block_base, int64_t row,
+                                                 int64_t rows, uint32_t& bad) {
+    if (row >= rows) return 0x7F7F7F7Fu;
+    if constexpr (KIND == SF_MX) return *reinterpret_cast<const uint32_t*>(slot + r * 16 + 4 * jj);
+    const int br = KIND == SF_ROW ? r : (int)(row >> 7) - block_base;
+    const float f = reinterpret_cast<const float*>(slot)[br * 4 + jj];
+    return e8m0_of_pow2(f, bad) * 0x01010101u;
+}
+
+template <int OUT_BF16, int KA, int KB>
+__global__ void __launch_bounds__(320, 1)
+    gemm_blockscaled_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                                 GemmArgs g, uint32_t idesc) {
+    extern __shared__ uint8_t smem_raw[];
+    SmemBsPair& S = *reinterpret_cast<SmemBsPair*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    const int groups = (g.k_tiles + 3) / 4;
+    volatile int* abort_flag = &S.abort_flag;
+    constexpr int kSaBytes = scale_box_rows<KA>(kPairRows) * 16;
+    constexpr int kSbBytes = scale_box_rows<KB>(BN_BS) * 16;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kBsPairStages; ++s) {
+            mbar_init(smem_u32(&S.full[s]), 2);     // one arrival per producer of the pair
+            mbar_init(smem_u32(&S.empty[s]), 1);    // the MMA commit
+            mbar_init(smem_u32(&S.sf_full[s]), 4);  // this CTA's four scale writers
+        }
+        for (int s = 0; s < kScaleSlots; ++s) {
+            mbar_init(smem_u32(&S.scale_full[s]), 1);
+            mbar_init(smem_u32(&S.scale_empty[s]), 4);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&S.tfull[a]), 1);
+            mbar_init(smem_u32(&S.tempty[a]), 8);
+        }
+        mbar_init(smem_u32(&S.drain), 1);
+        S.abort_flag = 0;
+        S.bad_scale = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmSA);
+        tma_prefetch_desc(&tmSB);
+    }
+    cluster_sync_all();
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&S.tmem_base), 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int issued = 0;                    // scale groups issued so far (flattened over this pair's tiles)
+            int nt = cid, ngrp = 0;            // the next (tile, group) whose scales to load
+            auto issue_next_scales = [&]() -> bool {
+                if (nt >= g.num_tiles || groups == 0) return true;
+                const int slot = issued % kScaleSlots;
+                if (issued >= kScaleSlots &&
+                    !mbar_wait_bounded(smem_u32(&S.scale_empty[slot]), (uint32_t)((issued / kScaleSlots - 1) & 1),
+                                       abort_flag))
+                    return false;
+                int tm, tn;
+                tile_coords(nt, g, tm, tn);
+                const int xa = KA == SF_MX ? 16 * ngrp : 4 * ngrp, xb = KB == SF_MX ? 16 * ngrp : 4 * ngrp;
+                const int arow = tm * kPairTile + (int)rank * kPairRows, brow = tn * BN_BS;
+                mbar_arrive_expect_tx(smem_u32(&S.scale_full[slot]), kSaBytes + kSbBytes);
+                tma_load_2d(smem_u32(S.sa[slot]), &tmSA, smem_u32(&S.scale_full[slot]), xa, KA == SF_BLOCK ? arow >> 7 : arow);
+                tma_load_2d(smem_u32(S.sb[slot]), &tmSB, smem_u32(&S.scale_full[slot]), xb, KB == SF_BLOCK ? brow >> 7 : brow);
+                ++issued;
+                if (++ngrp == groups) {
+                    ngrp = 0;
+                    nt += ncl;
+                }
+                return true;
+            };
+            for (int i = 0; ok && i < kScaleAhead; ++i) ok = issue_next_scales();
+            for (int t = cid; ok && t < g.num_tiles; t += ncl) {
+                int tm, tn;
+                tile_coords(t, g, tm, tn);
+                for (int kt = 0; kt < g.k_tiles; ++kt) {
+                    if ((kt & 3) == 0 && !(ok = issue_next_scales())) break;  // entering a group: keep two ahead
+                    if (!mbar_wait_bounded(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_leader = map_to_cta(smem_u32(&S.full[stage]), 0);
+                    tma_load_2d_pair(smem_u32(S.a[stage]), &tmA, full_leader, kt * BK, tm * kPairTile + (int)rank * kPairRows);
+                    tma_load_2d_pair(smem_u32(S.b[stage]), &tmB, full_leader, kt * BK, tn * BN_BS + (int)rank * kBsPairB);
+                    if (!mbar_wait_bounded(smem_u32(&S.sf_full[stage]), phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx_cluster(full_leader, kBsPairStageBytes);
+                    if (++stage == kBsPairStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 2000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = cid; ok && t < g.num_tiles; t += ncl) {
+                if (!mbar_wait_bounded(smem_u32(&S.tempty[acc]), acc_phase ^ 1, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * BN_BS);
+                for (int kt = 0; kt < g.k_tiles; ++kt) {
+                    if (!mbar_wait_bounded(smem_u32(&S.full[stage]), phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_kmajor_sw128(smem_u32(S.a[stage]));
+                    const uint64_t bd = sdesc_kmajor_sw128(smem_u32(S.b[stage]));
+                    const uint32_t sfa_t = tmem + (uint32_t)(kSfColBase + stage * kSfColsPerStage);
+                    const uint32_t sfb_t = sfa_t + 8;
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        tc_mma_mxf8f6f4_pair(d, ad + 2 * k, bd + 2 * k, idesc | ((uint32_t)k << 29) | ((uint32_t)k << 4),
+                                             sfa_t, sfb_t, (kt | k) != 0 ? 1u : 0u);
+                    tc_commit_pair_multicast(smem_u32(&S.empty[stage]), 0x3);
+                    if (++stage == kBsPairStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair_multicast(smem_u32(&S.tfull[acc]), 0x3);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            tc_commit_pair(smem_u32(&S.drain));
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&S.drain), 0))
+                if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+    } else if (warp < 6) {
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = cid; t < g.num_tiles; t += ncl) {
+            bool ok = mbar_wait_bounded(smem_u32(&S.tfull[acc]), acc_phase, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            int tm, tn;
+            tile_coords(t, g, tm, tn);
+            const int64_t row = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows + q * 32 + lane;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN_BS);
+#pragma unroll 1
+            for (int c = 0; c < BN_BS / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
+                const int64_t col0 = (int64_t)tn * BN_BS + c * 32;
+                if (row < g.M) store_row32<OUT_BF16>(g, row, col0, r, 1.0f, 1.0f);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&S.tempty[acc]), 0));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    } else {
+        // Scale writers of this CTA (warp 6..9 = lane quarter q): for every K tile, the A scale of rows
+        // 32q + lane (column q of the stage's slot) and the scales of all 224 B rows (columns 8 + j),
+        // read from the shared-memory scale ring.
+        const int q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        int stage = 0;
+        uint32_t phase = 0;
+        int consumed = 0;
+        uint32_t bad = 0;
+        bool ok = true;
+        for (int t = cid; ok && t < g.num_tiles; t += ncl) {
+            int tm, tn;
+            tile_coords(t, g, tm, tn);
+            const int64_t arow = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows + q * 32 + lane;
+            const int ablock = (tm * kPairTile + (int)rank * kPairRows) >> 7;
+            const int bblock = (tn * BN_BS) >> 7;
+            for (int grp = 0; ok && grp < groups; ++grp) {
+                const int slot = consumed % kScaleSlots;
+                bool w = mbar_wait_bounded(smem_u32(&S.scale_full[slot]), (uint32_t)((consumed / kScaleSlots) & 1), abort_flag);
+                if (!__all_sync(0xffffffffu, w)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    if (4 * grp + jj >= g.k_tiles) break;
+                    w = mbar_wait_bounded(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tslot = tmem + lane_base + (uint32_t)(kSfColBase + stage * kSfColsPerStage);
+                    tmem_st_32x32b_x1(tslot + q, sf_word_smem<KA>(S.sa[slot], q * 32 + lane, jj, ablock, arow, g.M, bad));
+                    uint32_t wb[8];
+#pragma unroll
+                    for (int j = 0; j < kSfbCols; ++j)
+                        wb[j] = sf_word_smem<KB>(S.sb[slot], 32 * j + lane, jj, bblock, (int64_t)tn * BN_BS + 32 * j + lane,
+                                                 g.N, bad);
+                    wb[7] = 0x7F7F7F7Fu;
+                    tmem_st_32x32b_x8(tslot + 8, wb);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&S.sf_full[stage]));
+                    if (++stage == kBsPairStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.scale_empty[slot]));
+                ++consumed;
+            }
+        }
+        if (__any_sync(0xffffffffu, bad != 0) && lane == 0) atomicOr(&S.bad_scale, 1);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
     if (threadIdx.x == 0 && g.status) {
         if (S.abort_flag) atomicOr(g.status, FP8_STATUS_TIMEOUT);
         if (S.bad_scale) atomicOr(g.status, FP8_STATUS_BAD_BLOCK_SCALE);
@@ -729,50 +1024,78 @@ fp8_status prepare_kernel(const void* func, size_t smem) {
     return FP8_OK;
 }
 
-template <int OUT_BF16>
-fp8_status launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g, uint32_t idesc,
-                       cudaStream_t st) {
-    auto k = gemm_tensor_pair_kernel<OUT_BF16>;
-    const size_t smem = sizeof(SmemPair) + 1024;
-    fp8_status s = prepare_kernel(reinterpret_cast<const void*>(k), smem);
-    if (s != FP8_OK) return s;
+// Number of pair tiles: the GemmArgs among the kernel arguments.
+template <typename... Rest>
+int pair_tiles_of(const GemmArgs& g, const Rest&...) { return g.num_tiles; }
+template <typename T, typename... Rest>
+int pair_tiles_of(const T&, const Rest&... rest) { return pair_tiles_of(rest...); }
+
+// 2-D map over a scale tensor for one group of four K tiles per row: 16 bytes per row (four E8M0
+// words' bytes, or four fp32), `box_rows` rows (or 128-row blocks for 128x128 scales).
+template <int KIND>
+fp8_status make_scale_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t ld, int tile_rows) {
+    auto fn = encode_fn();
+    FP8_REQUIRE(fn != nullptr, FP8_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    const bool mx = KIND == SF_MX;
+    const int64_t srows = KIND == SF_BLOCK ? (rows + 127) / 128 : rows;
+    cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)srows};
+    cuuint64_t strides[1] = {(cuuint64_t)(mx ? ld : 4 * ld)};
+    cuuint32_t box[2] = {(cuuint32_t)(mx ? 16 : 4), (cuuint32_t)scale_box_rows<KIND>(tile_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr),
+                    dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    FP8_REQUIRE(r == CUDA_SUCCESS, FP8_ERR_CUDA, "cuTensorMapEncodeTiled (scales) failed (%d)", (int)r);
+    return FP8_OK;
+}
+
+// Launch a CTA-pair kernel: clusters of 2, as many resident pairs as fit, never more pairs than tiles.
+template <typename Kernel, typename... Args>
+fp8_status launch_pair_kernel(Kernel k, size_t smem, int threads, cudaStream_t st, const Args&... args) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // one resident pair per two SMs (as many as fit), never more pairs than tiles
     static std::mutex mu;
-    static int max_clusters[64] = {0};
+    static std::map<std::pair<const void*, int>, int> max_pairs;  // (kernel, device) -> resident pairs
     int dev = 0;
     cudaGetDevice(&dev);
     int mc;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (dev < 0 || dev >= 64 || max_clusters[dev] == 0) {
+        auto key = std::make_pair(reinterpret_cast<const void*>(k), dev);
+        auto it = max_pairs.find(key);
+        if (it == max_pairs.end()) {
             cfg.gridDim = dim3(2 * (device_sm_count() / 2));
             int n = 0;
             if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k), &cfg) != cudaSuccess || n <= 0) {
                 cudaGetLastError();
                 n = device_sm_count() / 2;
             }
-            mc = n;
-            if (dev >= 0 && dev < 64) max_clusters[dev] = n;
-        } else {
-            mc = max_clusters[dev];
+            it = max_pairs.emplace(key, n).first;
         }
+        mc = it->second;
     }
-    const int pairs = std::max(1, std::min(g.num_tiles, mc));
+    const int pairs = std::max(1, std::min(pair_tiles_of(args...), mc));
     cfg.gridDim = dim3(2 * pairs);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k, tmA, tmB, g, idesc);
-    FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "gemm_tensor_pair_kernel launch: %s", cudaGetErrorString(e));
-    return check_launch("gemm_tensor_pair_kernel launch");
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, args...);
+    FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "CTA-pair GEMM launch: %s", cudaGetErrorString(e));
+    return check_launch("CTA-pair GEMM launch");
+}
+
+template <int OUT_BF16>
+fp8_status launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g, uint32_t idesc,
+                       cudaStream_t st) {
+    fp8_status s = prepare_kernel(reinterpret_cast<const void*>(gemm_tensor_pair_kernel<OUT_BF16>), sizeof(SmemPair) + 1024);
+    if (s != FP8_OK) return s;
+    return launch_pair_kernel(gemm_tensor_pair_kernel<OUT_BF16>, sizeof(SmemPair) + 1024, 192, st, tmA, tmB, g, idesc);
 }
 
 int sf_kind(int gran) { return gran == FP8_SCALE_MX_1x32 ? SF_MX : gran == FP8_SCALE_BLOCK_1x128 ? SF_ROW : SF_BLOCK; }
@@ -780,6 +1103,18 @@ int sf_kind(int gran) { return gran == FP8_SCALE_MX_1x32 ? SF_MX : gran == FP8_S
 template <int OUT_BF16, int KA, int KB>
 fp8_status launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g, uint32_t idesc, int grid,
                      cudaStream_t st) {
+    if (g.pair) {
+        CUtensorMap tmSA, tmSB;
+        fp8_status s = make_scale_map<KA>(&tmSA, g.sfa, g.M, g.sfa_ld, kPairRows);
+        if (s != FP8_OK) return s;
+        s = make_scale_map<KB>(&tmSB, g.sfb, g.N, g.sfb_ld, BN_BS);
+        if (s != FP8_OK) return s;
+        auto kp = gemm_blockscaled_pair_kernel<OUT_BF16, KA, KB>;
+        const size_t smem_p = sizeof(SmemBsPair) + 1024;
+        s = prepare_kernel(reinterpret_cast<const void*>(kp), smem_p);
+        if (s != FP8_OK) return s;
+        return launch_pair_kernel(kp, smem_p, 320, st, tmA, tmB, tmSA, tmSB, g, idesc);
+    }
     const size_t smem = sizeof(SmemBS) + 1024;
     auto k = gemm_blockscaled_kernel<OUT_BF16, KA, KB>;
     fp8_status s = prepare_kernel(reinterpret_cast<const void*>(k), smem);
@@ -812,7 +1147,10 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
                        const uint8_t* B, int64_t ldb, int fb, int gb, const void* sfb, void* D, int out_bf16,
                        int64_t ldd, int32_t* status, cudaStream_t st) {
     const bool blockscaled = ga != FP8_SCALE_TENSOR;
-    const bool pair = !blockscaled && M > BM;  // two-SM tiles once the second half of a 256-row tile has work
+    // two-SM tiles once the second half of a 256-row tile has work; block-scaled pairs TMA-load 16-byte
+    // scale rows, which needs K % 512 == 0 and 16-byte aligned scale tensors
+    const bool pair = M > BM && (!blockscaled || (K % 512 == 0 && (reinterpret_cast<uintptr_t>(sfa) & 15) == 0 &&
+                                                  (reinterpret_cast<uintptr_t>(sfb) & 15) == 0));
     const int bn = blockscaled ? BN_BS : BN;
     GemmArgs g;
     g.M = (int)M;
@@ -834,9 +1172,10 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
     CUtensorMap tmA, tmB;
     fp8_status s = make_operand_map(&tmA, A, M, K, lda, BM);
     if (s != FP8_OK) return s;
-    s = make_operand_map(&tmB, B, N, K, ldb, pair ? kPairRows : bn);
+    s = make_operand_map(&tmB, B, N, K, ldb, pair ? bn / 2 : bn);
     if (s != FP8_OK) return s;
-    if (pair) {
+    g.pair = pair;
+    if (pair && !blockscaled) {
         g.sa = static_cast<const float*>(sfa);
         g.sb = static_cast<const float*>(sfb);
         const uint32_t idesc = idesc_f8f6f4(fa, fb, kPairTile, BN);
@@ -870,7 +1209,7 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
     };
     g.vec_a = vec_ok(sfa, ga, g.sfa_ld);
     g.vec_b = vec_ok(sfb, gb, g.sfb_ld);
-    const uint32_t idesc = idesc_mxf8f6f4(fa, fb, BM, BN_BS, 0, 0);
+    const uint32_t idesc = idesc_mxf8f6f4(fa, fb, pair ? kPairTile : BM, BN_BS, 0, 0);
     return out_bf16 ? dispatch_bs<1>(sf_kind(ga), sf_kind(gb), tmA, tmB, g, idesc, grid, st)
                     : dispatch_bs<0>(sf_kind(ga), sf_kind(gb), tmA, tmB, g, idesc, grid, st);
 }
