@@ -80,7 +80,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -144,10 +144,10 @@ def run_ours(args, rank, world):
     c3 = BlockLinearFwd(d["X3"], d["W3"], mx=False, col=False)
 
     def c5_q(i):
-        x, st, qr, qc = [(c5.X, c5.sx, c5.qx_row, c5.qx_col), (c5.W, c5.sw, c5.qw_row, c5.qw_col),
-                         (c5.dY, c5.sg, c5.qg_row, c5.qg_col)][i]
-
         def f():
+            # operands looked up at call time: the end-to-end leg swaps the input buffers between steps
+            x, st, qr, qc = [(c5.X, c5.sx, c5.qx_row, c5.qx_col), (c5.W, c5.sw, c5.qw_row, c5.qw_col),
+                             (c5.dY, c5.sg, c5.qg_row, c5.qg_col)][i]
             if st.steps == 0:
                 from scaling_quantization_gemm_gb300.step import current_scaling
                 current_scaling(x, st)
@@ -257,30 +257,71 @@ def run_ours(args, rank, world):
 
 
 def run_e2e(args, d, host, ops, stream, c1, c5, c4, c3, step_flops, world):
+    """The step through the public API with host data: every step copies its inputs from pinned host
+    memory to the device and its results (all GEMM outputs) back to pinned host memory.  Like an
+    input pipeline, copies overlap computation: inputs and outputs are double-buffered on the device,
+    step i+1's inputs go up on one copy stream and step i-1's results come down on another while step
+    i computes on the compute stream; events order every reuse of a buffer."""
     import torch
     pinned_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory() for k, v in host.items()}
-    outs = [c1.Y, c5.Y, c5.dX, c5.dW, c4.Y, c3.Y]
-    pinned_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    out_names = [(c1, "Y"), (c5, "Y"), (c5, "dX"), (c5, "dW"), (c4, "Y"), (c3, "Y")]
+    in_names = {"X1": (c1, "X"), "W1": (c1, "W"), "X5": (c5, "X"), "W5": (c5, "W"), "dY5": (c5, "dY"),
+                "X4": (c4, "X"), "W4": (c4, "W"), "X3": (c3, "X"), "W3": (c3, "W")}
+    dev_in = [d, {k: torch.empty_like(v) for k, v in d.items()}]
+    dev_out = [[getattr(o, a) for o, a in out_names], [torch.empty_like(getattr(o, a)) for o, a in out_names]]
+    pinned_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out[0]]
     h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
     d2h = sum(t.numel() * t.element_size() for t in pinned_out)
-    steps = max(1, min(args.steps, args.e2e_steps))
+    steps = max(2, args.e2e_steps)
+    s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    h2d_done = [ev() for _ in range(steps)]
+    g_done = [ev() for _ in range(steps)]
+    d2h_done = [ev() for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def upload(i):
+        with torch.cuda.stream(s_h2d):
+            if i >= 2:
+                s_h2d.wait_event(g_done[i - 2])  # step i-2 no longer reads this input set
+            for k, t in pinned_in.items():
+                dev_in[i % 2][k].copy_(t, non_blocking=True)
+            h2d_done[i].record(s_h2d)
+
     barrier(world)
     torch.cuda.synchronize()
-    start.record(stream)
-    for _ in range(steps):
-        for k, t in pinned_in.items():
-            d[k].copy_(t, non_blocking=True)
+    start.record(s_h2d)
+    upload(0)
+    for i in range(steps):
+        if i + 1 < steps:
+            upload(i + 1)
+        k = i % 2
+        for name, (obj, attr) in in_names.items():
+            setattr(obj, attr, dev_in[k][name])
+        for (obj, attr), t in zip(out_names, dev_out[k]):
+            setattr(obj, attr, t)
+        stream.wait_event(h2d_done[i])
+        if i >= 2:
+            stream.wait_event(d2h_done[i - 2])  # step i-2's results have left this output set
         for _, f, *_ in ops:
             f()
-        for o, p in zip(outs, pinned_out):
-            p.copy_(o, non_blocking=True)
-    end.record(stream)
+        g_done[i].record(stream)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(g_done[i])
+            for t, p in zip(dev_out[k], pinned_out):
+                p.copy_(t, non_blocking=True)
+            d2h_done[i].record(s_d2h)
+    s_d2h.wait_event(d2h_done[steps - 1])
+    end.record(s_d2h)
     torch.cuda.synchronize()
+    for name, (obj, attr) in in_names.items():  # restore the resident buffers
+        setattr(obj, attr, dev_in[0][name])
+    for (obj, attr), t in zip(out_names, dev_out[0]):
+        setattr(obj, attr, t)
     ms = max_over_ranks(start.elapsed_time(end), world) / steps
     return {"value": round(step_flops * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 3),
-            "steps": steps}
+            "steps": steps, "copies": "overlapped with compute (double-buffered, two copy streams)"}
 
 
 def load_traffic(kernel: str):
@@ -464,10 +505,10 @@ def max_over_ranks(x: float, world: int) -> float:
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--reference-rows", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=sorted(PROFILE_CASES), default=None,
