@@ -699,9 +699,10 @@ __global__ void __launch_bounds__(320, 1)
 // B row n: lane 32q + n%32, column 8 + n/32, every quarter q).  The producer
 // TMA-loads the scales of each group of four K tiles (16 bytes per row: the A
 // rows of this CTA and all B rows of the tile) into a four-slot shared-memory
-// ring, two groups ahead; the writers read them there.  A producer arrives on the even CTA's
-// `full` barrier only after its own CTA's scale slot for that stage is written
-// (local `sf_full` barrier), so the even CTA's MMA sees the scales of both CTAs.
+// ring, two groups ahead; the writers read them there.  The even CTA's `full`
+// barrier of a stage completes when both producers' loads have landed and all
+// eight scale writers of the pair have written that stage's scale slot, so the
+// producers never wait for the writers.
 constexpr int kBsPairStages = 4;
 constexpr int kBsPairB = BN_BS / 2;                    // 112 rows of B per CTA
 constexpr int kBsPairABytes = kPairRows * BK;          // 16 KB
@@ -716,7 +717,7 @@ struct alignas(1024) SmemBsPair {
     uint8_t b[kBsPairStages][kBsPairBBytes];
     alignas(128) uint8_t sa[kScaleSlots][kPairRows * 16];  // per row: four K tiles x 4 bytes (E8M0 x4 or one fp32)
     alignas(128) uint8_t sb[kScaleSlots][BN_BS * 16];
-    uint64_t full[kBsPairStages], empty[kBsPairStages], sf_full[kBsPairStages], tfull[2], tempty[2], drain;
+    uint64_t full[kBsPairStages], empty[kBsPairStages], tfull[2], tempty[2], drain;
     uint64_t scale_full[kScaleSlots], scale_empty[kScaleSlots];
     uint32_t tmem_base;
     int abort_flag;
@@ -757,9 +758,8 @@ __global__ void __launch_bounds__(320, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBsPairStages; ++s) {
-            mbar_init(smem_u32(&S.full[s]), 2);     // one arrival per producer of the pair
-            mbar_init(smem_u32(&S.empty[s]), 1);    // the MMA commit
-            mbar_init(smem_u32(&S.sf_full[s]), 4);  // this CTA's four scale writers
+            mbar_init(smem_u32(&S.full[s]), 2 + 8);  // both producers + the eight scale writers of the pair
+            mbar_init(smem_u32(&S.empty[s]), 1);     // the MMA commit
         }
         for (int s = 0; s < kScaleSlots; ++s) {
             mbar_init(smem_u32(&S.scale_full[s]), 1);
@@ -829,10 +829,6 @@ __global__ void __launch_bounds__(320, 1)
                     const uint32_t full_leader = map_to_cta(smem_u32(&S.full[stage]), 0);
                     tma_load_2d_pair(smem_u32(S.a[stage]), &tmA, full_leader, kt * BK, tm * kPairTile + (int)rank * kPairRows);
                     tma_load_2d_pair(smem_u32(S.b[stage]), &tmB, full_leader, kt * BK, tn * BN_BS + (int)rank * kBsPairB);
-                    if (!mbar_wait_bounded(smem_u32(&S.sf_full[stage]), phase, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
                     mbar_arrive_expect_tx_cluster(full_leader, kBsPairStageBytes);
                     if (++stage == kBsPairStages) {
                         stage = 0;
@@ -956,7 +952,7 @@ __global__ void __launch_bounds__(320, 1)
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&S.sf_full[stage]));
+                    if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&S.full[stage]), 0));
                     if (++stage == kBsPairStages) {
                         stage = 0;
                         phase ^= 1;
