@@ -181,6 +181,39 @@ FP8Q_API fp8_status fp8_quantize(const void *x, int64_t rows, int64_t cols, int6
                         void *sf_row, void *sf_col, float *amax, void *stream);
 
 /*
+ * fp8_quantize_current -- per-tensor current scaling and the cast, in one launch.
+ * Source: FP8-AMAX scaling from the amax of the tensor being cast, the
+ * compute_bias rule, then the scaled cast ("Training and inference of large
+ * language models using 8-bit floating point", "Proposed method").
+ *
+ *   amax = max|x|;  e = compute_bias(amax, fmt, margin);  q = RNE_saturate_fmt(x * 2^e).
+ *
+ * The result is that of fp8_amax on a zeroed amax, then fp8_compute_scale,
+ * then fp8_quantize(FP8_SCALE_TENSOR) with the new scale, bit for bit; x is
+ * read twice, in one cooperative launch with a grid-wide barrier between the
+ * amax and the cast.
+ *
+ *   x, rows, cols, ld, fmt, q_row, q_col: as for fp8_quantize.
+ *   amax       device fp32 or NULL (written, not accumulated: max|x|).
+ *   bias, scale, scale_inv: device, or NULL, as for fp8_compute_scale.
+ *   workspace  device, FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES bytes, 16-byte
+ *              aligned, owned by the caller.  Zero it once before its first
+ *              use; every call leaves it ready for the next one.  Calls that
+ *              share a workspace must not run at the same time (same stream,
+ *              or ordered by events).  After a call that reported
+ *              FP8_STATUS_TIMEOUT, zero it again.
+ *   status     device int32 or NULL (FP8_STATUS_NONFINITE_AMAX,
+ *              FP8_STATUS_TIMEOUT: a CTA gave up waiting at the barrier and
+ *              the codes are not valid).
+ * An empty x writes amax 0, bias 0, scale 1, scale_inv 1.
+ */
+#define FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES 4096
+FP8Q_API fp8_status fp8_quantize_current(const void *x, int64_t rows, int64_t cols, int64_t ld, fp8_format fmt,
+                                         int32_t margin, uint8_t *q_row, uint8_t *q_col, float *amax, int32_t *bias,
+                                         float *scale, float *scale_inv, void *workspace, int32_t *status,
+                                         void *stream);
+
+/*
  * fp8_scaled_gemm -- D = unscale(A . B^T) on FP8 operands.
  * Source: the unscaling step that follows the FP8 matrix product ("Training
  * and inference of large language models using 8-bit floating point",

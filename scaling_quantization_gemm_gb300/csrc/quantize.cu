@@ -155,8 +155,10 @@ __device__ __forceinline__ void store_col32(uint8_t* q_col, int64_t c, int64_t r
 // cross-warp reduction (128x128 blocks, 128x1 column blocks).  Row pass: thread t holds the 16-byte chunk column j = t % 16 of
 // rows t/16 + 16 i, i = 0..7.  Column pass: warp w covers column pairs
 // lane + 32 (w & 1) over the 32-row segment w / 2.
+// The tile loop (shared by the cast kernel and the fused current-scaling kernel).  For
+// per-tensor scaling `s_given` is the scale; block granularities compute their own.
 template <int GRAN, int FMT>
-__global__ void __launch_bounds__(kThreads, 3) quantize_tile_kernel(const __grid_constant__ CUtensorMap tmX, QuantArgs a) {
+__device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const QuantArgs& a, float s_given) {
     extern __shared__ uint8_t smem_raw[];
     QuantSmem& S = *reinterpret_cast<QuantSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -179,12 +181,12 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_tile_kernel(const __grid
         const int64_t tile = blockIdx.x + i * gridDim.x;
         const int st = (int)(i % kQStages);
         mbar_arrive_expect_tx(smem_u32(&S.full[st]), kTile * kTile * 2);
-        tma_load_2d(smem_u32(S.tile[st]), &tmX, smem_u32(&S.full[st]), (int)((tile % a.tiles_c) * kTile),
+        tma_load_2d(smem_u32(S.tile[st]), tmX, smem_u32(&S.full[st]), (int)((tile % a.tiles_c) * kTile),
                     (int)((tile / a.tiles_c) * kTile));
     };
     int64_t issued = 0;  // meaningful in thread 0
     if (tid == 0) {
-        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(tmX);
         for (; issued < kQStages && issued < n_my; ++issued) issue(issued);
     }
 
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_tile_kernel(const __grid
     bool pow2_tensor = true;
     if constexpr (GRAN == FP8_SCALE_TENSOR) {
         // a positive normal power of two 2^e is exact as a bf16x2 pair; any other scale takes the fp32 path
-        s_tensor = *a.scale;
+        s_tensor = s_given;
         const uint32_t u = __float_as_uint(s_tensor);
         pow2_tensor = (u & 0x807FFFFFu) == 0 && (u >> 23) - 1u < 254u;
         const uint32_t sb = u >> 16;
@@ -392,6 +394,117 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_tile_kernel(const __grid
     }
 }
 
+template <int GRAN, int FMT>
+__global__ void __launch_bounds__(kThreads, 3) quantize_tile_kernel(const __grid_constant__ CUtensorMap tmX, QuantArgs a) {
+    quantize_tiles<GRAN, FMT>(&tmX, a, GRAN == FP8_SCALE_TENSOR ? *a.scale : 1.0f);
+}
+
+// ------------------------------------------------- fused current scaling
+
+// Per-tensor current scaling in one cooperative launch: amax of x, the
+// compute_bias rule, and the cast with 2^e.  Phase 1 reduces max|x| per CTA
+// into the workspace; the last CTA to reach the grid barrier reduces those,
+// derives e, writes the caller's amax / bias / scale / scale_inv, publishes 2^e
+// and releases the others (a generation counter, so the workspace is left
+// ready for the next call); phase 2 is the tile loop of the cast kernel.
+struct CurrentWorkspace {
+    unsigned count;   // CTAs arrived at the barrier of the current call
+    unsigned gen;     // barrier generation
+    float scale;      // 2^e of the current call
+    unsigned pad;
+    unsigned partial[1];  // per-CTA max |x| (bf16 magnitude bits), one per CTA
+};
+constexpr int kCurrentWsHeader = 16;
+constexpr int kCurrentMaxCtas = (FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES - kCurrentWsHeader) / 4;
+
+struct CurrentOut {
+    float* amax;
+    int32_t* bias;
+    float* scale;
+    float* scale_inv;
+    int32_t* status;
+    int margin;
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 3)
+    quantize_current_kernel(const __grid_constant__ CUtensorMap tmX, QuantArgs a, const uint16_t* x, int64_t ld,
+                            CurrentOut out, CurrentWorkspace* ws) {
+    __shared__ uint32_t red[kThreads / 32];
+    __shared__ float s_scale;
+    __shared__ int s_abort;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // phase 1: max |x| of this CTA's share of 16-byte chunks
+    const int64_t cpr = a.cols >> 3;
+    const int64_t total = a.rows * cpr;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    auto addr = [&](int64_t id) -> const uint16_t* {
+        return (ld == a.cols) ? x + id * 8 : x + (id / cpr) * ld + (id % cpr) * 8;
+    };
+    uint32_t m = 0;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + tid;
+    for (; i + 3 * stride < total; i += 4 * stride) {
+        const uint4 v0 = ld_stream_v4(addr(i)), v1 = ld_stream_v4(addr(i + stride));
+        const uint4 v2 = ld_stream_v4(addr(i + 2 * stride)), v3 = ld_stream_v4(addr(i + 3 * stride));
+        m = absmax2(absmax2(absmax2(absmax2(m, v0.x), v0.y), v0.z), v0.w);
+        m = absmax2(absmax2(absmax2(absmax2(m, v1.x), v1.y), v1.z), v1.w);
+        m = absmax2(absmax2(absmax2(absmax2(m, v2.x), v2.y), v2.z), v2.w);
+        m = absmax2(absmax2(absmax2(absmax2(m, v3.x), v3.y), v3.z), v3.w);
+    }
+    for (; i < total; i += stride) {
+        const uint4 v = ld_stream_v4(addr(i));
+        m = absmax2(absmax2(absmax2(absmax2(m, v.x), v.y), v.z), v.w);
+    }
+    m = __reduce_max_sync(0xffffffffu, fold2(m));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+
+    // grid barrier (bounded wait), scale selection by the last CTA
+    if (tid == 0) {
+        uint32_t mx = red[0];
+        for (int w = 1; w < kThreads / 32; ++w) mx = max(mx, red[w]);
+        volatile CurrentWorkspace* vws = ws;
+        const unsigned gen0 = vws->gen;
+        vws->partial[blockIdx.x] = mx;
+        __threadfence();
+        s_abort = 0;
+        if (atomicAdd(&ws->count, 1u) == gridDim.x - 1) {
+            __threadfence();
+            uint32_t all = 0;
+            for (unsigned c = 0; c < gridDim.x; ++c) all = max(all, vws->partial[c]);
+            const float amax = bf16bits_to_float(all);
+            bool nf = false;
+            const int e = bias_from_amax(amax, FMT, out.margin, &nf);
+            if (out.amax) *out.amax = amax;
+            if (out.bias) *out.bias = e;
+            if (out.scale) *out.scale = pow2_exact(e);
+            if (out.scale_inv) *out.scale_inv = pow2_exact(-e);
+            if (nf && out.status) atomicOr(out.status, FP8_STATUS_NONFINITE_AMAX);
+            vws->scale = pow2_exact(e);
+            vws->count = 0;
+            __threadfence();
+            atomicAdd(&ws->gen, 1u);
+        } else {
+            const uint64_t t0 = globaltimer_ns();
+            while (vws->gen == gen0) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    s_abort = 1;
+                    if (out.status) atomicOr(out.status, FP8_STATUS_TIMEOUT);
+                    break;
+                }
+            }
+            __threadfence();
+        }
+        s_scale = vws->scale;
+    }
+    __syncthreads();
+    if (s_abort) return;
+
+    // phase 2: the cast
+    quantize_tiles<FP8_SCALE_TENSOR, FMT>(&tmX, a, s_scale);
+}
+
 // Standalone amax: grid-stride over 16-byte chunks, four loads in flight per thread.
 __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* amax) {
     const int64_t cpr = cols >> 3;
@@ -547,20 +660,76 @@ fp8_status launch_history(float* hist, int len, int64_t* pos, float* amax, int f
     return check_launch("history kernel launch");
 }
 
-fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int gran, int margin,
-                           const float* scale, uint8_t* q_row, uint8_t* q_col, void* sf_row, void* sf_col,
-                           float* amax, cudaStream_t st) {
+namespace {
+
+// bf16 [rows x cols] (row stride ld) in 128 x 128 boxes, no swizzle.
+fp8_status make_x_map(const void* x, int64_t rows, int64_t cols, int64_t ld, CUtensorMap* tm) {
     auto fn = q_encode_fn();
     FP8_REQUIRE(fn != nullptr, FP8_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-    CUtensorMap tm;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
     cuuint32_t box[2] = {(cuuint32_t)kTile, (cuuint32_t)kTile};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     FP8_REQUIRE(r == CUDA_SUCCESS, FP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return FP8_OK;
+}
+
+__global__ void current_empty_kernel(CurrentOut out) {
+    if (out.amax) *out.amax = 0.0f;
+    if (out.bias) *out.bias = 0;
+    if (out.scale) *out.scale = 1.0f;
+    if (out.scale_inv) *out.scale_inv = 1.0f;
+}
+
+template <int FMT>
+fp8_status launch_current(const CUtensorMap& tm, const QuantArgs& a, const void* x, int64_t ld, const CurrentOut& out,
+                          void* workspace, cudaStream_t st) {
+    auto k = quantize_current_kernel<FMT>;
+    const size_t smem = sizeof(QuantSmem) + 1024;
+    static std::mutex mu;
+    static int occ_dev[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int occ;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || occ_dev[dev] == 0) {
+            cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            int o = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k, kThreads, smem);
+            FP8_REQUIRE(o > 0, FP8_ERR_CUDA, "current-scaling kernel does not fit on an SM");
+            occ = o;
+            if (dev >= 0 && dev < 64) occ_dev[dev] = occ;
+        } else {
+            occ = occ_dev[dev];
+        }
+    }
+    // every CTA must be resident at once (grid barrier): at most SMs x occupancy, and one
+    // workspace slot per CTA
+    int64_t grid = (int64_t)device_sm_count() * occ;
+    if (grid > a.ntiles) grid = a.ntiles;
+    if (grid > kCurrentMaxCtas) grid = kCurrentMaxCtas;
+    if (grid < 1) grid = 1;
+    CUtensorMap tm_arg = tm;
+    QuantArgs a_arg = a;
+    const uint16_t* x_arg = static_cast<const uint16_t*>(x);
+    int64_t ld_arg = ld;
+    CurrentOut out_arg = out;
+    CurrentWorkspace* ws_arg = static_cast<CurrentWorkspace*>(workspace);
+    void* args[] = {&tm_arg, &a_arg, &x_arg, &ld_arg, &out_arg, &ws_arg};
+    cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k), dim3((unsigned)grid),
+                                                dim3(kThreads), args, smem, st);
+    FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cooperative launch: %s", cudaGetErrorString(e));
+    return FP8_OK;
+}
+
+QuantArgs quant_args(int64_t rows, int64_t cols, int margin, const float* scale, uint8_t* q_row, uint8_t* q_col,
+                     void* sf_row, void* sf_col, float* amax) {
     QuantArgs a;
     a.rows = rows;
     a.cols = cols;
@@ -576,6 +745,18 @@ fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld
     a.do_row = q_row != nullptr;
     a.do_col = q_col != nullptr;
     a.status = nullptr;
+    return a;
+}
+
+}  // namespace
+
+fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int gran, int margin,
+                           const float* scale, uint8_t* q_row, uint8_t* q_col, void* sf_row, void* sf_col,
+                           float* amax, cudaStream_t st) {
+    CUtensorMap tm;
+    fp8_status s = make_x_map(x, rows, cols, ld, &tm);
+    if (s != FP8_OK) return s;
+    const QuantArgs a = quant_args(rows, cols, margin, scale, q_row, q_col, sf_row, sf_col, amax);
 #define FP8Q_QDISPATCH(G)                                                         \
     case G:                                                                       \
         return fmt == FP8_E4M3 ? launch_quant<G, FP8_E4M3>(tm, a, st) : launch_quant<G, FP8_E5M2>(tm, a, st);
@@ -587,6 +768,23 @@ fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld
     }
 #undef FP8Q_QDISPATCH
     return FP8_ERR_UNSUPPORTED;
+}
+
+fp8_status launch_quantize_current(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int margin,
+                                   uint8_t* q_row, uint8_t* q_col, float* amax, int32_t* bias, float* scale,
+                                   float* scale_inv, void* workspace, int32_t* status, cudaStream_t st) {
+    const CurrentOut out{amax, bias, scale, scale_inv, status, margin};
+    if (rows == 0 || cols == 0) {
+        current_empty_kernel<<<1, 1, 0, st>>>(out);
+        return check_launch("current-scaling kernel launch");
+    }
+    CUtensorMap tm;
+    fp8_status s = make_x_map(x, rows, cols, ld, &tm);
+    if (s != FP8_OK) return s;
+    QuantArgs a = quant_args(rows, cols, margin, nullptr, q_row, q_col, nullptr, nullptr, nullptr);
+    a.status = status;
+    return fmt == FP8_E4M3 ? launch_current<FP8_E4M3>(tm, a, x, ld, out, workspace, st)
+                           : launch_current<FP8_E5M2>(tm, a, x, ld, out, workspace, st);
 }
 
 }  // namespace fp8q

@@ -9,12 +9,13 @@ buffers are torch tensors; torch is only the allocator.
 * ``ScaleState`` holds one tensor's scaling state on the device: the amax
   accumulator, bias, scale 2^e and scale_inv 2^-e, plus the amax history ring
   and its position for delayed scaling.
-* ``current_scaling`` runs amax -> compute_scale (the FP8-AMAX rule).
+* ``current_scaling`` runs amax -> compute_scale (the FP8-AMAX rule);
+  ``quantize_current`` does that and the cast in one fused launch.
 * ``LinearFwdBwd`` is one FP8 linear layer, forward and backward, with
   per-tensor delayed scaling: quantise X, W (E4M3) and dY (E5M2) row- and
   column-wise with the fused amax, run fprop / dgrad / wgrad, then advance
   the three histories.  On its first step a history is empty, so that step
-  uses current scaling (amax pass first).
+  uses current scaling (the fused amax + scale + cast).
 * ``BlockLinearFwd`` is the forward with per-block (1x128 activations,
   128x128 weights) or MXFP8 (1x32, E8M0) scales.
 """
@@ -25,8 +26,9 @@ from typing import Optional
 
 import torch
 
-from . import (BLOCK_1x128, BLOCK_128x128, DGRAD, E4M3, E5M2, FPROP, MX_1x32, TENSOR, WGRAD, fp8_amax,
-               fp8_amax_history_update, fp8_compute_scale, fp8_quantize, fp8_scaled_gemm)
+from . import (BLOCK_1x128, BLOCK_128x128, DGRAD, E4M3, E5M2, FPROP, MX_1x32, TENSOR, WGRAD, current_workspace,
+               fp8_amax, fp8_amax_history_update, fp8_compute_scale, fp8_quantize, fp8_quantize_current,
+               fp8_scaled_gemm)
 
 
 class ScaleState:
@@ -56,6 +58,12 @@ def current_scaling(x: torch.Tensor, st: ScaleState) -> None:
     st.amax.zero_()
 
 
+def quantize_current(x: torch.Tensor, st: ScaleState, ws: torch.Tensor, q_row=None, q_col=None) -> None:
+    """Current scaling and the cast in one launch: st.amax = max|x|, st.bias/scale/scale_inv from it."""
+    fp8_quantize_current(x, st.fmt, st.margin, ws, q_row=q_row, q_col=q_col, amax=st.amax, bias=st.bias,
+                         scale=st.scale, scale_inv=st.scale_inv, status=st.status)
+
+
 def gemm_flops(m: int, n: int, k: int) -> float:
     return 2.0 * m * n * k
 
@@ -75,13 +83,12 @@ class PerTensorFwd:
         self.qx = torch.empty(M, K, dtype=torch.uint8, device=dev)
         self.qw = torch.empty(N, K, dtype=torch.uint8, device=dev)
         self.Y = torch.empty(M, N, dtype=torch.float32, device=dev)
+        self.ws = current_workspace(dev)
         self.flops = gemm_flops(M, N, K)
 
     def run(self) -> None:
-        current_scaling(self.X, self.sx)
-        current_scaling(self.W, self.sw)
-        fp8_quantize(self.X, E4M3, TENSOR, scale=self.sx.scale, q_row=self.qx)
-        fp8_quantize(self.W, E4M3, TENSOR, scale=self.sw.scale, q_row=self.qw)
+        quantize_current(self.X, self.sx, self.ws, q_row=self.qx)
+        quantize_current(self.W, self.sw, self.ws, q_row=self.qw)
         fp8_scaled_gemm(FPROP, self.qx, E4M3, TENSOR, self.sx.scale_inv, self.qw, E4M3, TENSOR, self.sw.scale_inv,
                         self.Y)
 
@@ -112,15 +119,21 @@ class LinearFwdBwd:
         self.Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         self.dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
         self.dW = torch.empty(N, K, dtype=dw_dtype, device=dev)
+        self.ws = current_workspace(dev)
         self.flops = 3 * gemm_flops(M, N, K)
         self.quant_bytes = 4 * (M * K + N * K + M * N)  # 2 B read + 1 B row + 1 B col per element
 
-    def quantize(self) -> None:
-        for x, st, qr, qc in ((self.X, self.sx, self.qx_row, self.qx_col), (self.W, self.sw, self.qw_row, self.qw_col),
-                              (self.dY, self.sg, self.qg_row, self.qg_col)):
-            if st.steps == 0:
-                current_scaling(x, st)  # empty history: this step scales from its own amax
+    def quantize_one(self, i: int) -> None:
+        x, st, qr, qc = ((self.X, self.sx, self.qx_row, self.qx_col), (self.W, self.sw, self.qw_row, self.qw_col),
+                         (self.dY, self.sg, self.qg_row, self.qg_col))[i]
+        if st.steps == 0:
+            quantize_current(x, st, self.ws, q_row=qr, q_col=qc)  # empty history: scale from its own amax
+        else:
             fp8_quantize(x, st.fmt, TENSOR, scale=st.scale, q_row=qr, q_col=qc, amax=st.amax)
+
+    def quantize(self) -> None:
+        for i in range(3):
+            self.quantize_one(i)
 
     def gemms(self) -> None:
         fp8_scaled_gemm(FPROP, self.qx_row, E4M3, TENSOR, self.sx.scale_inv, self.qw_row, E4M3, TENSOR,

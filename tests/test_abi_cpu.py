@@ -27,9 +27,10 @@ def declared_symbols():
     return sorted(set(re.findall(r"\b(fp8_[a-z_0-9]+)\s*\(", text)))
 
 
-def test_header_declares_the_five_calls():
+def test_header_declares_the_entry_points():
     syms = declared_symbols()
-    for s in ["fp8_amax", "fp8_compute_scale", "fp8_amax_history_update", "fp8_quantize", "fp8_scaled_gemm"]:
+    for s in ["fp8_amax", "fp8_compute_scale", "fp8_amax_history_update", "fp8_quantize", "fp8_quantize_current",
+              "fp8_scaled_gemm"]:
         assert s in syms
 
 
@@ -113,3 +114,25 @@ def test_gemm_validation(L):
     assert g(*args(ga=3, gb=3, K=160, lda=160, ldb=160)) == 2  # block-scaled needs K % 128
     assert g(*args(lda=64)) == 1  # lda < K
     assert g(*args(M=0)) == 0  # empty output: no-op
+
+
+def test_quantize_current_validation(L):
+    qc = L.fp8_quantize_current
+    a = lambda **kw: [kw.get("x", FAKE), kw.get("rows", 32), kw.get("cols", 32), kw.get("ld", 32), kw.get("fmt", 0),
+                      0, kw.get("q_row", FAKE), kw.get("q_col", None), FAKE, FAKE, FAKE, FAKE, kw.get("ws", FAKE),
+                      None, None]
+    assert qc(*a(ws=None)) == 1
+    assert "workspace" in _detail(L)
+    assert qc(*a(ws=FAKE + 8)) == 1  # workspace not 16-byte aligned
+    assert qc(*a(fmt=3)) == 1
+    assert qc(*a(q_row=None)) == 1  # no output
+    assert qc(*a(ld=16)) == 1  # ld < cols
+    assert qc(*a(cols=12, ld=12)) == 2
+    assert qc(*a(rows=24, q_col=FAKE)) == 2  # column-wise output needs rows % 16
+
+
+def test_workspace_size_constant_matches_header(L):
+    import scaling_quantization_gemm_gb300 as q
+    text = open(HEADER).read()
+    m = re.search(r"#define FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES (\d+)", text)
+    assert m and int(m.group(1)) == q.QUANTIZE_CURRENT_WORKSPACE_BYTES
