@@ -214,6 +214,33 @@ FP8Q_API fp8_status fp8_quantize_current(const void *x, int64_t rows, int64_t co
                                          void *stream);
 
 /*
+ * fp8_quantize_current_noalloc -- fp8_quantize_current without a workspace.
+ * No counterpart in the method's sources: this entry point exists for callers
+ * that cannot allocate device memory where they call it (a plugin or callback
+ * given only its input and output buffers by a host framework, code whose
+ * device memory is planned once against a fixed budget, loops that cannot
+ * take the synchronisation cudaMalloc / cudaFree may cause).  It allocates
+ * nothing.
+ *
+ * Arguments and results are those of fp8_quantize_current, without
+ * `workspace`.  The scratch is a static 4 KB array in the library's device
+ * code, present on every GPU that loads the library until the process exits.
+ * It holds one slot per CTA, at most 1020 CTAs; a launch that would need more
+ * returns FP8_ERR_UNSUPPORTED.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - Every call shares the array and finds the previous call's contents in
+ *     it; each call clears the barrier header on its stream first.  Calls
+ *     whose kernels overlap on the GPU (different streams or host threads)
+ *     race on the array: order them.
+ */
+FP8Q_API fp8_status fp8_quantize_current_noalloc(const void *x, int64_t rows, int64_t cols, int64_t ld,
+                                                 fp8_format fmt, int32_t margin, uint8_t *q_row, uint8_t *q_col,
+                                                 float *amax, int32_t *bias, float *scale, float *scale_inv,
+                                                 int32_t *status, void *stream);
+
+/*
  * fp8_scaled_gemm -- D = unscale(A . B^T) on FP8 operands.
  * Source: the unscaling step that follows the FP8 matrix product ("Training
  * and inference of large language models using 8-bit floating point",

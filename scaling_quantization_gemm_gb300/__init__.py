@@ -33,7 +33,7 @@ STATUS_NONFINITE_AMAX, STATUS_TIMEOUT, STATUS_BAD_BLOCK_SCALE = 1, 2, 4
 
 # every entry point declared in include/fp8q.h
 ENTRY_POINTS = ("fp8_amax", "fp8_compute_scale", "fp8_amax_history_update", "fp8_quantize", "fp8_quantize_current",
-                "fp8_scaled_gemm", "fp8_status_string", "fp8_last_error_detail")
+                "fp8_quantize_current_noalloc", "fp8_scaled_gemm", "fp8_status_string", "fp8_last_error_detail")
 QUANTIZE_CURRENT_WORKSPACE_BYTES = 4096  # FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES
 
 
@@ -63,6 +63,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_amax_history_update": [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp],
                 "fp8_quantize": [vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp],
                 "fp8_quantize_current": [vp, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+                "fp8_quantize_current_noalloc": [vp, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp],
                 "fp8_scaled_gemm": [i32, i64, i64, i64, vp, i64, i32, i32, vp, vp, i64, i32, i32, vp, vp, i32, i64,
                                     vp, vp],
             }.items():
@@ -154,6 +155,16 @@ def fp8_quantize_current(x: torch.Tensor, fmt: int, margin: int, workspace: Ptr,
                                       _p(scale), _p(scale_inv), _p(workspace), _p(status), _stream(stream)))
 
 
+def fp8_quantize_current_noalloc(x: torch.Tensor, fmt: int, margin: int, q_row: Ptr = None, q_col: Ptr = None,
+                                 amax: Ptr = None, bias: Ptr = None, scale: Ptr = None, scale_inv: Ptr = None,
+                                 status: Ptr = None, stream=None) -> None:
+    """fp8_quantize_current with the library's static scratch instead of a workspace (allocates nothing)."""
+    rows, cols, ld = _matrix(x)
+    _check("fp8_quantize_current_noalloc",
+           lib().fp8_quantize_current_noalloc(_p(x), rows, cols, ld, fmt, margin, _p(q_row), _p(q_col), _p(amax),
+                                              _p(bias), _p(scale), _p(scale_inv), _p(status), _stream(stream)))
+
+
 def fp8_scaled_gemm(op: int, A: torch.Tensor, fa: int, ga: int, sfa: Ptr, B: torch.Tensor, fb: int, gb: int,
                     sfb: Ptr, D: torch.Tensor, status: Ptr = None, stream=None) -> None:
     """D[M x N] = unscale(A[M x K] . B[N x K]^T); out dtype from D (float32 or bfloat16)."""
@@ -170,6 +181,7 @@ def fp8_scaled_gemm(op: int, A: torch.Tensor, fa: int, ga: int, sfa: Ptr, B: tor
 
 
 __all__ = ["lib", "FP8Error", "status_name", "fp8_amax", "fp8_compute_scale", "fp8_amax_history_update",
-           "fp8_quantize", "fp8_quantize_current", "current_workspace", "fp8_scaled_gemm", "ENTRY_POINTS",
+           "fp8_quantize", "fp8_quantize_current", "fp8_quantize_current_noalloc",
+           "current_workspace", "fp8_scaled_gemm", "ENTRY_POINTS",
            "QUANTIZE_CURRENT_WORKSPACE_BYTES", "LIB_PATH", "E4M3", "E5M2", "TENSOR", "BLOCK_1x128",
            "BLOCK_128x128", "MX_1x32", "FPROP", "DGRAD", "WGRAD", "OUT_F32", "OUT_BF16"]

@@ -26,6 +26,9 @@ fp8_status launch_history(float* hist, int len, int64_t* pos, float* amax, int f
 fp8_status launch_quantize_current(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int margin,
                                    uint8_t* q_row, uint8_t* q_col, float* amax, int32_t* bias, float* scale,
                                    float* scale_inv, void* workspace, int32_t* status, cudaStream_t st);
+fp8_status launch_quantize_current_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt,
+                                           int margin, uint8_t* q_row, uint8_t* q_col, float* amax, int32_t* bias,
+                                           float* scale, float* scale_inv, int32_t* status, cudaStream_t st);
 fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int gran, int margin,
                            const float* scale, uint8_t* q_row, uint8_t* q_col, void* sf_row, void* sf_col,
                            float* amax, cudaStream_t st);
@@ -159,6 +162,29 @@ fp8_status fp8_quantize_current(const void* x, int64_t rows, int64_t cols, int64
     }
     return launch_quantize_current(x, rows, cols, ld, fmt, margin, q_row, q_col, amax, bias, scale, scale_inv,
                                    workspace, status, as_stream(stream));
+}
+
+fp8_status fp8_quantize_current_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld, fp8_format fmt,
+                                        int32_t margin, uint8_t* q_row, uint8_t* q_col, float* amax, int32_t* bias,
+                                        float* scale, float* scale_inv, int32_t* status, void* stream) {
+    g_detail[0] = 0;
+    fp8_status s = check_bf16_matrix(x, rows, cols, ld);
+    if (s != FP8_OK) return s;
+    FP8_REQUIRE(valid_fmt(fmt), FP8_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
+    FP8_REQUIRE((!amax || aligned(amax, 4)) && (!bias || aligned(bias, 4)) && (!scale || aligned(scale, 4)) &&
+                    (!scale_inv || aligned(scale_inv, 4)) && (!status || aligned(status, 4)),
+                FP8_ERR_INVALID_ARG, "amax, bias, scale, scale_inv and status must be 4-byte aligned");
+    if (rows > 0 && cols > 0) {
+        FP8_REQUIRE(q_row || q_col, FP8_ERR_INVALID_ARG, "q_row and q_col are both NULL");
+        FP8_REQUIRE(!q_row || aligned(q_row, 8), FP8_ERR_UNSUPPORTED, "q_row must be 8-byte aligned");
+        if (q_col) {
+            FP8_REQUIRE(rows % 16 == 0, FP8_ERR_UNSUPPORTED,
+                        "column-wise output needs rows %% 16 == 0 (rows=%lld)", (long long)rows);
+            FP8_REQUIRE(aligned(q_col, 16), FP8_ERR_UNSUPPORTED, "q_col must be 16-byte aligned");
+        }
+    }
+    return launch_quantize_current_noalloc(x, rows, cols, ld, fmt, margin, q_row, q_col, amax, bias, scale,
+                                           scale_inv, status, as_stream(stream));
 }
 
 fp8_status fp8_scaled_gemm(fp8_gemm_op op, int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,

@@ -787,4 +787,118 @@ fp8_status launch_quantize_current(const void* x, int64_t rows, int64_t cols, in
                            : launch_current<FP8_E5M2>(tm, a, x, ld, out, workspace, st);
 }
 
+// ------------------------------------------- fused current scaling, no allocation
+//
+// fp8_quantize_current_noalloc runs the same kernel as fp8_quantize_current, with
+// its barrier counters and per-CTA partials in the library's own static device
+// array instead of a caller workspace.  It is for callers that cannot allocate
+// device memory at the point of the call: a plugin or callback that a host
+// framework hands only its input and output buffers, code whose device memory is
+// planned once at start-up against a fixed budget, and latency-bound loops that
+// cannot take the device-wide synchronisation cudaMalloc / cudaFree may cause.
+//
+// The array is kNoAllocScratchBytes (4 KB) on every GPU that loads the library,
+// held until the process exits: a 16-byte header (arrival count, generation,
+// scale) and one 4-byte partial per CTA, so at most (4096 - 16) / 4 = 1020 CTAs.
+// A launch that would need more is rejected.  Every call shares the array and
+// finds the previous call's contents there; the call clears the header on its
+// stream before the kernel, and each CTA writes its partial before any CTA reads
+// it.  Calls whose kernels overlap on the GPU (other streams, other host threads)
+// race on the array.
+constexpr int kNoAllocScratchBytes = 4096;
+static __device__ __align__(256) unsigned char g_current_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+// Device address of g_current_scratch on the current device.  In host code the
+// array's name only stands for the symbol; the first call on each device looks
+// its address up, with that device current, and caches it.
+fp8_status noalloc_scratch(void** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    FP8_REQUIRE(dev >= 0 && dev < 64, FP8_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_current_scratch);
+        FP8_REQUIRE(e == cudaSuccess && p != nullptr, FP8_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s",
+                    cudaGetErrorString(e));
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return FP8_OK;
+}
+
+template <int FMT>
+fp8_status launch_current_noalloc(const CUtensorMap& tm, const QuantArgs& a, const void* x, int64_t ld,
+                                  const CurrentOut& out, void* scratch, cudaStream_t st) {
+    auto k = quantize_current_kernel<FMT>;
+    const size_t smem = sizeof(QuantSmem) + 1024;
+    static std::mutex mu;
+    static int occ_dev[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int occ;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || occ_dev[dev] == 0) {
+            cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            int o = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k, kThreads, smem);
+            FP8_REQUIRE(o > 0, FP8_ERR_CUDA, "current-scaling kernel does not fit on an SM");
+            occ = o;
+            if (dev >= 0 && dev < 64) occ_dev[dev] = occ;
+        } else {
+            occ = occ_dev[dev];
+        }
+    }
+    int64_t grid = (int64_t)device_sm_count() * occ;  // all CTAs resident at once (grid barrier)
+    if (grid > a.ntiles) grid = a.ntiles;
+    if (grid < 1) grid = 1;
+    const int64_t need = kCurrentWsHeader + 4 * grid;
+    FP8_REQUIRE(need <= kNoAllocScratchBytes, FP8_ERR_UNSUPPORTED,
+                "this launch needs %lld bytes of scratch (%lld CTAs); the static array holds %d bytes (%d CTAs)",
+                (long long)need, (long long)grid, kNoAllocScratchBytes, (kNoAllocScratchBytes - kCurrentWsHeader) / 4);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, kCurrentWsHeader, st);
+    FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaMemsetAsync(scratch header): %s", cudaGetErrorString(e));
+    CUtensorMap tm_arg = tm;
+    QuantArgs a_arg = a;
+    const uint16_t* x_arg = static_cast<const uint16_t*>(x);
+    int64_t ld_arg = ld;
+    CurrentOut out_arg = out;
+    CurrentWorkspace* ws_arg = static_cast<CurrentWorkspace*>(scratch);
+    void* args[] = {&tm_arg, &a_arg, &x_arg, &ld_arg, &out_arg, &ws_arg};
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k), dim3((unsigned)grid), dim3(kThreads), args,
+                                    smem, st);
+    FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cooperative launch: %s", cudaGetErrorString(e));
+    return FP8_OK;
+}
+
+}  // namespace
+
+fp8_status launch_quantize_current_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt,
+                                           int margin, uint8_t* q_row, uint8_t* q_col, float* amax, int32_t* bias,
+                                           float* scale, float* scale_inv, int32_t* status, cudaStream_t st) {
+    const CurrentOut out{amax, bias, scale, scale_inv, status, margin};
+    if (rows == 0 || cols == 0) {
+        current_empty_kernel<<<1, 1, 0, st>>>(out);
+        return check_launch("current-scaling kernel launch");
+    }
+    void* scratch = nullptr;
+    fp8_status s = noalloc_scratch(&scratch);
+    if (s != FP8_OK) return s;
+    CUtensorMap tm;
+    s = make_x_map(x, rows, cols, ld, &tm);
+    if (s != FP8_OK) return s;
+    QuantArgs a = quant_args(rows, cols, margin, nullptr, q_row, q_col, nullptr, nullptr, nullptr);
+    a.status = status;
+    return fmt == FP8_E4M3 ? launch_current_noalloc<FP8_E4M3>(tm, a, x, ld, out, scratch, st)
+                           : launch_current_noalloc<FP8_E5M2>(tm, a, x, ld, out, scratch, st);
+}
+
 }  // namespace fp8q

@@ -136,3 +136,15 @@ def test_workspace_size_constant_matches_header(L):
     text = open(HEADER).read()
     m = re.search(r"#define FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES (\d+)", text)
     assert m and int(m.group(1)) == q.QUANTIZE_CURRENT_WORKSPACE_BYTES
+
+
+def test_quantize_current_noalloc_validation(L):
+    qn = L.fp8_quantize_current_noalloc
+    a = lambda **kw: [kw.get("x", FAKE), kw.get("rows", 32), kw.get("cols", 32), kw.get("ld", 32), kw.get("fmt", 0),
+                      0, kw.get("q_row", FAKE), kw.get("q_col", None), FAKE, FAKE, FAKE, FAKE, None, None]
+    assert qn(*a(fmt=3)) == 1
+    assert qn(*a(q_row=None)) == 1
+    assert qn(*a(x=None)) == 1
+    assert qn(*a(ld=16)) == 1
+    assert qn(*a(cols=12, ld=12)) == 2
+    assert qn(*a(rows=24, q_col=FAKE)) == 2
