@@ -218,6 +218,8 @@ def run_ours(args, rank, world):
     traffic = load_traffic("gemm_tensor_pair_kernel")
     peak_note = f"{'sustained' if long_loop else 'burst'} bf16 x {FP8_OVER_BF16:g} (nominal fp8/bf16), {pk_src}"
 
+    nxt = measure_next_rows(args, dev, c5, pk, stream) if not args.no_next_rows else None
+
     cpu = cpu_baseline(host) if (rank == 0 and not args.no_cpu_baseline) else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -239,6 +241,7 @@ def run_ours(args, rank, world):
                                  "per_block_tflops": round(blk_tflops, 1),
                                  "per_block_frac": round(blk_tflops / fp8_peak, 4)},
         "breakdown_ms": {k: round(v, 4) for k, v in per_op.items()},
+        "next_rows": nxt,
         "device_status": status,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -247,6 +250,83 @@ def run_ours(args, rank, world):
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def _time_op(f, reps: int, stream, warmup: int = 3) -> float:
+    """Mean device ms of f() over `reps` launches (events on the launching stream), after warm-up."""
+    import torch
+    for _ in range(warmup):
+        f()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        f()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def measure_next_rows(args, dev, c5, pk, stream):
+    """The rows beyond the training step, each on its own, outside the timed step: the fused
+    current-scaling cast, the fixed-bias (FP8-CSCALE) sweep statistics, and post-training-quantised
+    inference through two FP8 linear layers with the hidden cast fused into GEMM 1's epilogue."""
+    import torch
+
+    import scaling_quantization_gemm_gb300 as q
+    import workloads as wl
+    from scaling_quantization_gemm_gb300.step import PTQStack, bias_sweep
+    hbm = pk["hbm_gbs"]
+    fp8_peak = pk["bf16_tflops"] * FP8_OVER_BF16
+    out = {}
+
+    # fused current scaling, row + column casts of X (16384 x 5120): 2 B amax read + 2 B read + 2 x 1 B
+    x = c5.X
+    qr, qc = torch.empty_like(c5.qx_row), torch.empty_like(c5.qx_col)
+    ws = q.current_workspace(dev)
+    o = [torch.zeros(1, device=dev) for _ in range(3)] + [torch.zeros(1, dtype=torch.int32, device=dev)]
+    ms = _time_op(lambda: q.fp8_quantize_current(x, q.E4M3, 0, ws, q_row=qr, q_col=qc, amax=o[0], scale=o[1],
+                                                 scale_inv=o[2], bias=o[3]), 20, stream)
+    gbs = 6.0 * x.numel() / (ms * 1e-3) / 1e9
+    out["current_scaling_fused"] = {"kernel": "quantize_current_kernel (E4M3, row+col)", "shape": list(x.shape),
+                                    "ms": round(ms, 4), "achieved": round(gbs, 1), "unit": "GB/s",
+                                    "peak": hbm, "frac": round(gbs / hbm, 4), "bytes_per_elem": 6}
+
+    # fixed-bias sweep e in [-3, 3] over the E5M2 gradient dY (16384 x 20480): one pass, 2 B / element
+    y = c5.dY
+    scales = torch.empty(7, device=dev)
+    for j, e in enumerate(range(-3, 4)):
+        q.fp8_set_bias(e, scale=scales[j:j + 1])
+    sat = torch.zeros(7, dtype=torch.int64, device=dev)
+    und = torch.zeros(7, dtype=torch.int64, device=dev)
+    ms = _time_op(lambda: q.fp8_cast_stats(y, q.E5M2, scales, sat, und), 20, stream)
+    gbs = 2.0 * y.numel() / (ms * 1e-3) / 1e9
+    sweep = bias_sweep(y, q.E5M2, range(-3, 4))
+    out["cscale_sweep_stats"] = {"kernel": "cast_stats_kernel (7 fixed biases, E5M2)", "shape": list(y.shape),
+                                 "ms": round(ms, 4), "achieved": round(gbs, 1), "unit": "GB/s", "peak": hbm,
+                                 "frac": round(gbs / hbm, 4), "bytes_per_elem": 2,
+                                 "underflow_frac_by_e": {r["e"]: round(r["underflow_frac"], 6) for r in sweep}}
+
+    # PTQ inference: 8192 tokens through 5120 -> 13824 -> 5120, hidden cast in GEMM 1's epilogue
+    Xb, W1b, W2b = wl.ptq_ffn()
+    to = lambda b: torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
+    Xd = to(Xb)
+    stack = PTQStack(to(W1b), to(W2b), Xb.shape[0], act="current")
+    stack.forward(Xd)  # first forward: no hidden history yet (bf16 GEMM 1 + current scaling)
+    ms = _time_op(lambda: stack.forward(Xd), 20, stream)
+    T, F = stack.T, stack.F
+    g1 = lambda: q.fp8_scaled_gemm_quantize(q.FPROP, stack.qx, q.E4M3, stack.sx.scale_inv, stack.qw1, q.E4M3,
+                                            stack.sw1.scale_inv, stack.qh, q.E4M3, stack.sh.scale, stack.sh.amax)
+    ms_g1 = _time_op(g1, 20, stream)
+    tf_g1 = 2.0 * T * F * stack.H / (ms_g1 * 1e-3) / 1e12
+    out["ptq_ffn_inference"] = {
+        "workload": "8192 tokens, 13B FFN 5120 -> 13824 -> 5120, PTQ weights, current-scaled input",
+        "ms_per_forward": round(ms, 4), "tflops": round(stack.flops / (ms * 1e-3) / 1e12, 1),
+        "fused_epilogue_gemm": {"kernel": "gemm_tensor_pair_kernel<E4M3 out> (GEMM 1 + hidden cast + amax)",
+                                "ms": round(ms_g1, 4), "achieved": round(tf_g1, 1), "unit": "TFLOP/s",
+                                "peak": round(fp8_peak, 1), "frac": round(tf_g1 / fp8_peak, 4)},
+        "status": int(stack.sh.status.item())}
+    return out
 
 
 def run_e2e(args, d, host, ops, stream, c1, c5, c4, c3, step_flops, world):
@@ -429,7 +509,32 @@ def run_case(name: str, launches: int = 3) -> None:
     torch.cuda.set_device(0)
     g = torch.Generator(device="cuda").manual_seed(0)
     kind, shape = PROFILE_CASES[name]
-    if kind.startswith("gemm"):
+    if kind == "gemm_quant":
+        M, N, K = shape
+        A = torch.randint(0, 0x7E, (M, K), dtype=torch.uint8, device="cuda", generator=g)
+        B = torch.randint(0, 0x7E, (N, K), dtype=torch.uint8, device="cuda", generator=g)
+        Dq = torch.empty(M, N, dtype=torch.uint8, device="cuda")
+        s = torch.full((1,), 2.0 ** -8, device="cuda")
+        amax = torch.zeros(1, device="cuda")
+        for _ in range(launches):
+            q.fp8_scaled_gemm_quantize(q.FPROP, A, 0, s, B, 0, s, Dq, 0, s, amax)
+    elif kind == "quant_current":
+        R, C = shape
+        x = torch.randn(R, C, device="cuda", generator=g).to(torch.bfloat16)
+        qr = torch.empty(R, C, dtype=torch.uint8, device="cuda")
+        qc = torch.empty(C, R, dtype=torch.uint8, device="cuda")
+        ws = q.current_workspace()
+        for _ in range(launches):
+            q.fp8_quantize_current(x, 0, 0, ws, q_row=qr, q_col=qc)
+    elif kind == "cast_stats":
+        R, C = shape
+        x = torch.randn(R, C, device="cuda", generator=g).to(torch.bfloat16)
+        sc = torch.exp2(torch.arange(-3, 4, device="cuda").float())
+        sat = torch.zeros(7, dtype=torch.int64, device="cuda")
+        und = torch.zeros(7, dtype=torch.int64, device="cuda")
+        for _ in range(launches):
+            q.fp8_cast_stats(x, 1, sc, sat, und)
+    elif kind.startswith("gemm"):
         M, N, K = shape
         A = torch.randint(0, 0x7E, (M, K), dtype=torch.uint8, device="cuda", generator=g)
         B = torch.randint(0, 0x7E, (N, K), dtype=torch.uint8, device="cuda", generator=g)
@@ -473,6 +578,9 @@ PROFILE_CASES = {
     "gemm_ffn_fprop": ("gemm_tensor", (16384, 20480, 5120)),
     "quant_tensor": ("quant_tensor", (16384, 8192)),
     "quant_mx": ("quant_mx", (16384, 8192)),
+    "gemm_fused_q": ("gemm_quant", (8192, 13824, 5120)),
+    "quant_current": ("quant_current", (16384, 5120)),
+    "cast_stats": ("cast_stats", (16384, 8192)),
 }
 
 
@@ -504,6 +612,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--reference-rows", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true", help="skip the rows measured beside the step")
     ap.add_argument("--case", choices=sorted(PROFILE_CASES), default=None,
                     help="run one kernel on a small (> L2) case for an ncu capture, then exit")
     args = ap.parse_args(argv)

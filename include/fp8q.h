@@ -140,6 +140,43 @@ FP8Q_API fp8_status fp8_amax_history_update(float *history, int32_t len, int64_t
                                    int32_t *status, void *stream);
 
 /*
+ * fp8_set_bias -- a fixed exponent bias (FP8-CSCALE).
+ * Source: fixed scaling, a bias chosen once per tensor instead of derived
+ * from its amax, compared against FP8-AMAX in a sweep of fixed values
+ * ("Training and inference of large language models using 8-bit floating
+ * point", "Proposed method" and "Key findings").
+ *
+ *   bias = e; scale = 2^e; scale_inv = 2^-e.    e in [-126, 127], else INVALID_ARG.
+ *   bias, scale, scale_inv: device, each may be NULL (not all three).
+ * The outputs feed fp8_quantize and fp8_scaled_gemm like those of
+ * fp8_compute_scale.
+ */
+FP8Q_API fp8_status fp8_set_bias(int32_t e, int32_t *bias, float *scale, float *scale_inv, void *stream);
+
+/*
+ * fp8_cast_stats -- what a cast at given scales does to a tensor.
+ * Source: the range problem fixed scaling runs into, overflow and underflow
+ * of the FP8 range ("Training and inference of large language models using
+ * 8-bit floating point", "Motivation & Objective" and "Key findings", the
+ * fixed-scaling sweep).
+ *
+ *   for j < n:  saturated[j] += #{ x not NaN : |fl32(x * scales[j])| > fmax }
+ *               underflow[j] += #{ x not NaN, x != 0 : cast of fl32(x * scales[j]) is +-0 }
+ *
+ *   x          as for fp8_amax (bf16 [rows x cols], ld, 16-byte aligned, cols
+ *              and ld multiples of 8).
+ *   fmt        the format the cast targets (fmax 448 or 57344).
+ *   scales     device fp32[n], 1 <= n <= 8 (any values; powers of two from
+ *              fp8_set_bias or fp8_compute_scale in the usual case).
+ *   saturated, underflow: device uint64[n], ACCUMULATED (the caller zeroes them).
+ * The counts are exactly what fp8_quantize would clip and flush with that
+ * scale.  Empty x is a no-op.
+ */
+FP8Q_API fp8_status fp8_cast_stats(const void *x, int64_t rows, int64_t cols, int64_t ld, fp8_format fmt,
+                                   const float *scales, int32_t n, uint64_t *saturated, uint64_t *underflow,
+                                   void *stream);
+
+/*
  * fp8_quantize -- the scaled cast to FP8, row-wise and/or column-wise.
  * Source: the scaling step that precedes the FP8 cast ("Training and
  * inference of large language models using 8-bit floating point", "Proposed
@@ -275,6 +312,36 @@ FP8Q_API fp8_status fp8_scaled_gemm(fp8_gemm_op op, int64_t M, int64_t N, int64_
                            fp8_format fa, fp8_granularity ga, const void *sfa, const uint8_t *B, int64_t ldb,
                            fp8_format fb, fp8_granularity gb, const void *sfb, void *D, fp8_out_dtype out_dtype,
                            int64_t ldd, int32_t *status, void *stream);
+
+/*
+ * fp8_scaled_gemm_quantize -- per-tensor FP8 GEMM whose epilogue casts D to FP8.
+ * Source: in a stack of FP8 linear layers the output of one layer is the
+ * input the next one scales and casts, and its scale comes from its amax
+ * ("Training and inference of large language models using 8-bit floating
+ * point", "Proposed method"); here that cast, and the amax, are done where
+ * D leaves the accumulator.
+ *
+ *   v[m, n]  = ((sum_k A[m,k] B[n,k]) * sa) * sb     (fp32 accumulation, fp32 products)
+ *   Dq[m, n] = RNE_saturate_fd(v[m, n] * scale_d)     (one rounding, as fp8_quantize)
+ *   amax_d   = max(amax_d, max |v|)                    (accumulated, like fp8_amax)
+ *
+ *   A, lda, fa, B, ldb, fb: as for fp8_scaled_gemm; sfa / sfb point to one fp32
+ *            each (per-tensor dequantisation factors 2^-e).
+ *   Dq       device u8 [M x N], leading dimension ldd (bytes); 16-byte aligned,
+ *            N and ldd multiples of 16.
+ *   fd       format of Dq.
+ *   scale_d  device, one fp32: the scale of Dq (2^e; with delayed scaling the
+ *            one fp8_amax_history_update chose from earlier steps).
+ *   amax_d   device fp32 or NULL: max |v| is folded in (to be recorded by
+ *            fp8_amax_history_update).  A NaN in v makes it NaN.
+ *   status   device int32 or NULL (FP8_STATUS_TIMEOUT).
+ * K == 0 writes zero codes and leaves amax_d unchanged.
+ */
+FP8Q_API fp8_status fp8_scaled_gemm_quantize(fp8_gemm_op op, int64_t M, int64_t N, int64_t K, const uint8_t *A,
+                                             int64_t lda, fp8_format fa, const float *sfa, const uint8_t *B,
+                                             int64_t ldb, fp8_format fb, const float *sfb, uint8_t *Dq, int64_t ldd,
+                                             fp8_format fd, const float *scale_d, float *amax_d, int32_t *status,
+                                             void *stream);
 
 /* fp8_status_string -- static, human-readable name of a status code. */
 FP8Q_API const char *fp8_status_string(fp8_status s);

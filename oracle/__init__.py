@@ -19,6 +19,10 @@ What each function computes, and the passage it follows, is stated in
   Training", "Key Questions Answered").
 * ``history_update`` -- delayed scaling from an amax window (same page).
 * ``gemm_sample`` / ``gemm_full`` -- fp64 product of the dequantised operands.
+* ``gemm_quantize_bracket`` -- the FP8 codes a GEMM whose output is cast for the
+  next layer may write (the cast of "Proposed method" applied to D).
+* ``cast_stats`` -- how many elements a given (e.g. fixed, FP8-CSCALE) scale
+  saturates and flushes to zero.
 
 Every function here is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_*.py`` against closed forms, exhaustive tables, brute force
@@ -79,6 +83,7 @@ def lib() -> ctypes.CDLL:
             L.fp8o_quantize_block.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp]
             L.fp8o_history_update.restype = i32
             L.fp8o_history_update.argtypes = [vp, ctypes.c_int32, vp, vp, i32, i32, vp, vp, vp]
+            L.fp8o_cast_stats.argtypes = [vp, i64, i64, i64, i32, vp, i32, vp, vp]
             L.fp8o_gemm_sample.argtypes = [i64, i64, i64, vp, i64, i32, i32, vp, vp, i64, i32, i32, vp,
                                            i64, vp, vp, vp, vp]
             L.fp8o_gemm_full.argtypes = [i64, i64, i64, vp, i64, i32, i32, vp, vp, i64, i32, i32, vp, vp, vp]
@@ -268,3 +273,43 @@ def gemm_tolerance(y_ref: np.ndarray, mag: np.ndarray, out_bf16: bool) -> np.nda
         ulp = np.where(a > 0, np.ldexp(1.0, (x - 1 - 7).astype(np.int64)), 0.0)
         tol = tol + 0.5 * ulp
     return tol
+
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """fp32 values rounded to the nearest bf16 (ties to even), returned as fp32; NaN stays NaN."""
+    u = np.ascontiguousarray(v, np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    out = r.astype(np.uint32).view(np.float32)
+    return np.where(np.isnan(v), np.float32(np.nan), out)
+
+
+def gemm_quantize_bracket(y_ref: np.ndarray, tol: np.ndarray, fmt: int, scale_d: float, via_bf16: bool = False):
+    """Codes a GEMM with an FP8 output may write: Encode(fl32(v * scale_d)) for some fp32 v with
+    |v - y_ref| <= tol (with via_bf16, v is first rounded to bf16: a bf16 output cast afterwards).
+    Encode, the fp32 product and the bf16 rounding are monotone in v, so the admissible codes are
+    exactly those between the codes of the two ends of the interval (the ends rounded outward to
+    fp32 never narrow it).  Returns (lo, hi, nearest): code arrays for y_ref - tol, y_ref + tol
+    and y_ref itself."""
+    s = np.float32(scale_d)
+    y_ref = np.asarray(y_ref, np.float64)
+    tol = np.asarray(tol, np.float64)
+
+    def codes(v):
+        v32 = np.asarray(v, np.float64).astype(np.float32)
+        if via_bf16:
+            v32 = round_bf16(v32)
+        return encode_array(v32 * s, fmt)
+
+    return codes(y_ref - tol), codes(y_ref + tol), codes(y_ref)
+
+
+def cast_stats(x_bf16: np.ndarray, fmt: int, scales) -> tuple[np.ndarray, np.ndarray]:
+    """(saturated[j], underflow[j]) for each scale s_j: elements with |fl32(x s_j)| > fmax, and
+    non-zero elements whose cast is +-0 (NaN elements count in neither)."""
+    x = np.ascontiguousarray(x_bf16).view(np.uint16)
+    sc = np.ascontiguousarray(scales, np.float32).reshape(-1)
+    sat = np.zeros(sc.size, np.uint64)
+    und = np.zeros(sc.size, np.uint64)
+    lib().fp8o_cast_stats(_p(x), x.shape[0], x.shape[1], x.shape[1], fmt, _p(sc), sc.size, _p(sat), _p(und))
+    return sat, und
+

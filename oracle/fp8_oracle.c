@@ -356,6 +356,36 @@ void fp8o_gemm_full(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t l
         }
 }
 
+/* ----------------------------------------------------- cast statistics */
+
+/* FP8-CSCALE keeps one fixed bias per tensor instead of deriving it from the
+ * amax, and fixed biases work only in a narrow range ("Training and inference
+ * of large language models using 8-bit floating point", "Proposed method" and
+ * "Key findings": the fixed-scaling sweep).  What a fixed scale does to a
+ * tensor is counted here by definition, for each scale s_j:
+ *   saturated[j] += #{ x : x not NaN, |fl32(x s_j)| > fmax }   (the cast clips it)
+ *   underflow[j] += #{ x : x not NaN, x != 0, Encode(fl32(x s_j)) = +-0 }  (flushed)
+ * Counts are accumulated into the caller's arrays. */
+void fp8o_cast_stats(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld, int fmt, const float *scales,
+                     int n, uint64_t *saturated, uint64_t *underflow)
+{
+    const double fmax = fmt_max(fmt);
+    for (int j = 0; j < n; ++j) {
+        uint64_t sat = 0, und = 0;
+#pragma omp parallel for reduction(+ : sat, und) schedule(static)
+        for (int64_t r = 0; r < rows; ++r)
+            for (int64_t c = 0; c < cols; ++c) {
+                const float xv = bf16_value(x[r * ld + c]);
+                if (isnan(xv)) continue;
+                const float v = xv * scales[j];
+                if (!isnan(v) && fabs((double)v) > fmax) ++sat;
+                if (xv != 0.0f && (fp8o_encode(v, fmt) & 0x7F) == 0) ++und;
+            }
+        saturated[j] += sat;
+        underflow[j] += und;
+    }
+}
+
 /* ------------------------------------------------------------ threads */
 
 int fp8o_max_threads(void)

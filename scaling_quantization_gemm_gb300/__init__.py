@@ -32,8 +32,9 @@ OUT_F32, OUT_BF16 = 0, 1
 STATUS_NONFINITE_AMAX, STATUS_TIMEOUT, STATUS_BAD_BLOCK_SCALE = 1, 2, 4
 
 # every entry point declared in include/fp8q.h
-ENTRY_POINTS = ("fp8_amax", "fp8_compute_scale", "fp8_amax_history_update", "fp8_quantize", "fp8_quantize_current",
-                "fp8_quantize_current_noalloc", "fp8_scaled_gemm", "fp8_status_string", "fp8_last_error_detail")
+ENTRY_POINTS = ("fp8_amax", "fp8_compute_scale", "fp8_amax_history_update", "fp8_set_bias", "fp8_cast_stats",
+                "fp8_quantize", "fp8_quantize_current",
+                "fp8_quantize_current_noalloc", "fp8_scaled_gemm", "fp8_scaled_gemm_quantize", "fp8_status_string", "fp8_last_error_detail")
 QUANTIZE_CURRENT_WORKSPACE_BYTES = 4096  # FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES
 
 
@@ -62,10 +63,14 @@ def lib() -> ctypes.CDLL:
                 "fp8_compute_scale": [vp, i32, i32, vp, vp, vp, vp, vp],
                 "fp8_amax_history_update": [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp],
                 "fp8_quantize": [vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp],
+                "fp8_set_bias": [i32, vp, vp, vp, vp],
+                "fp8_cast_stats": [vp, i64, i64, i64, i32, vp, i32, vp, vp, vp],
                 "fp8_quantize_current": [vp, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp],
                 "fp8_quantize_current_noalloc": [vp, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp],
                 "fp8_scaled_gemm": [i32, i64, i64, i64, vp, i64, i32, i32, vp, vp, i64, i32, i32, vp, vp, i32, i64,
                                     vp, vp],
+                "fp8_scaled_gemm_quantize": [i32, i64, i64, i64, vp, i64, i32, vp, vp, i64, i32, vp, vp, i64, i32, vp,
+                                             vp, vp, vp],
             }.items():
                 f = getattr(L, name)
                 f.argtypes = args
@@ -133,6 +138,19 @@ def fp8_amax_history_update(history: torch.Tensor, pos: Ptr, amax: Ptr, fmt: int
                                          _p(scale), _p(scale_inv), _p(status), _stream(stream)))
 
 
+def fp8_set_bias(e: int, bias: Ptr = None, scale: Ptr = None, scale_inv: Ptr = None, stream=None) -> None:
+    """A fixed (FP8-CSCALE) bias: bias = e, scale = 2^e, scale_inv = 2^-e on the device."""
+    _check("fp8_set_bias", lib().fp8_set_bias(int(e), _p(bias), _p(scale), _p(scale_inv), _stream(stream)))
+
+
+def fp8_cast_stats(x: torch.Tensor, fmt: int, scales: torch.Tensor, saturated: torch.Tensor, underflow: torch.Tensor,
+                   stream=None) -> None:
+    """Accumulate, per scale, the elements the cast would saturate and flush to zero (int64 counters)."""
+    rows, cols, ld = _matrix(x)
+    _check("fp8_cast_stats", lib().fp8_cast_stats(_p(x), rows, cols, ld, fmt, _p(scales), scales.numel(),
+                                                  _p(saturated), _p(underflow), _stream(stream)))
+
+
 def fp8_quantize(x: torch.Tensor, fmt: int, gran: int, margin: int = 0, scale: Ptr = None, q_row: Ptr = None,
                  q_col: Ptr = None, sf_row: Ptr = None, sf_col: Ptr = None, amax: Ptr = None, stream=None) -> None:
     rows, cols, ld = _matrix(x)
@@ -180,8 +198,25 @@ def fp8_scaled_gemm(op: int, A: torch.Tensor, fa: int, ga: int, sfa: Ptr, B: tor
                                                     _p(sfb), _p(D), out, ldd, _p(status), _stream(stream)))
 
 
+def fp8_scaled_gemm_quantize(op: int, A: torch.Tensor, fa: int, sfa: Ptr, B: torch.Tensor, fb: int, sfb: Ptr,
+                             Dq: torch.Tensor, fd: int, scale_d: Ptr, amax_d: Ptr = None, status: Ptr = None,
+                             stream=None) -> None:
+    """Dq[M x N] (u8) = RNE_sat(unscale(A . B^T) * scale_d); max |unscale(A . B^T)| folded into amax_d."""
+    M, K, lda = _matrix(A)
+    N, K2, ldb = _matrix(B)
+    if K != K2:
+        raise ValueError("A and B disagree on K")
+    Dm, Dn, ldd = _matrix(Dq)
+    if (Dm, Dn) != (M, N) or Dq.dtype != torch.uint8:
+        raise ValueError("Dq must be uint8 [M x N]")
+    _check("fp8_scaled_gemm_quantize",
+           lib().fp8_scaled_gemm_quantize(op, M, N, K, _p(A), lda, fa, _p(sfa), _p(B), ldb, fb, _p(sfb), _p(Dq), ldd,
+                                          fd, _p(scale_d), _p(amax_d), _p(status), _stream(stream)))
+
+
 __all__ = ["lib", "FP8Error", "status_name", "fp8_amax", "fp8_compute_scale", "fp8_amax_history_update",
+           "fp8_set_bias", "fp8_cast_stats",
            "fp8_quantize", "fp8_quantize_current", "fp8_quantize_current_noalloc",
-           "current_workspace", "fp8_scaled_gemm", "ENTRY_POINTS",
+           "current_workspace", "fp8_scaled_gemm", "fp8_scaled_gemm_quantize", "ENTRY_POINTS",
            "QUANTIZE_CURRENT_WORKSPACE_BYTES", "LIB_PATH", "E4M3", "E5M2", "TENSOR", "BLOCK_1x128",
            "BLOCK_128x128", "MX_1x32", "FPROP", "DGRAD", "WGRAD", "OUT_F32", "OUT_BF16"]

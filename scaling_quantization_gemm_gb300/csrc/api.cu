@@ -29,12 +29,15 @@ fp8_status launch_quantize_current(const void* x, int64_t rows, int64_t cols, in
 fp8_status launch_quantize_current_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt,
                                            int margin, uint8_t* q_row, uint8_t* q_col, float* amax, int32_t* bias,
                                            float* scale, float* scale_inv, int32_t* status, cudaStream_t st);
+fp8_status launch_set_bias(int e, int32_t* bias, float* scale, float* scale_inv, cudaStream_t st);
+fp8_status launch_cast_stats(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, const float* scales,
+                             int n, uint64_t* saturated, uint64_t* underflow, cudaStream_t st);
 fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int gran, int margin,
                            const float* scale, uint8_t* q_row, uint8_t* q_col, void* sf_row, void* sf_col,
                            float* amax, cudaStream_t st);
 fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, int fa, int ga, const void* sfa,
-                       const uint8_t* B, int64_t ldb, int fb, int gb, const void* sfb, void* D, int out_bf16,
-                       int64_t ldd, int32_t* status, cudaStream_t st);
+                       const uint8_t* B, int64_t ldb, int fb, int gb, const void* sfb, void* D, int out,
+                       int64_t ldd, const float* sd, float* amax_d, int32_t* status, cudaStream_t st);
 
 namespace {
 
@@ -187,6 +190,29 @@ fp8_status fp8_quantize_current_noalloc(const void* x, int64_t rows, int64_t col
                                            scale_inv, status, as_stream(stream));
 }
 
+fp8_status fp8_set_bias(int32_t e, int32_t* bias, float* scale, float* scale_inv, void* stream) {
+    g_detail[0] = 0;
+    FP8_REQUIRE(e >= -126 && e <= 127, FP8_ERR_INVALID_ARG, "bias %d outside [-126, 127]", (int)e);
+    FP8_REQUIRE(bias || scale || scale_inv, FP8_ERR_INVALID_ARG, "bias, scale and scale_inv are all NULL");
+    FP8_REQUIRE((!bias || aligned(bias, 4)) && (!scale || aligned(scale, 4)) && (!scale_inv || aligned(scale_inv, 4)),
+                FP8_ERR_INVALID_ARG, "bias, scale and scale_inv must be 4-byte aligned");
+    return launch_set_bias(e, bias, scale, scale_inv, as_stream(stream));
+}
+
+fp8_status fp8_cast_stats(const void* x, int64_t rows, int64_t cols, int64_t ld, fp8_format fmt, const float* scales,
+                          int32_t n, uint64_t* saturated, uint64_t* underflow, void* stream) {
+    g_detail[0] = 0;
+    fp8_status s = check_bf16_matrix(x, rows, cols, ld);
+    if (s != FP8_OK) return s;
+    FP8_REQUIRE(valid_fmt(fmt), FP8_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
+    FP8_REQUIRE(n >= 1 && n <= 8, FP8_ERR_INVALID_ARG, "n = %d scales (1 to 8)", (int)n);
+    FP8_REQUIRE(scales && saturated && underflow, FP8_ERR_INVALID_ARG, "scales, saturated and underflow are required");
+    FP8_REQUIRE(aligned(scales, 4) && aligned(saturated, 8) && aligned(underflow, 8), FP8_ERR_INVALID_ARG,
+                "scales must be 4-byte and the counters 8-byte aligned");
+    if (rows == 0 || cols == 0) return FP8_OK;
+    return launch_cast_stats(x, rows, cols, ld, fmt, scales, n, saturated, underflow, as_stream(stream));
+}
+
 fp8_status fp8_scaled_gemm(fp8_gemm_op op, int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
                            fp8_format fa, fp8_granularity ga, const void* sfa, const uint8_t* B, int64_t ldb,
                            fp8_format fb, fp8_granularity gb, const void* sfb, void* D, fp8_out_dtype out_dtype,
@@ -224,8 +250,41 @@ fp8_status fp8_scaled_gemm(fp8_gemm_op op, int64_t M, int64_t N, int64_t K, cons
     } else {
         FP8_REQUIRE(aligned(sfa, 4) && aligned(sfb, 4), FP8_ERR_INVALID_ARG, "sfa/sfb must be 4-byte aligned");
     }
-    return launch_gemm(M, N, K, A, lda, fa, ga, sfa, B, ldb, fb, gb, sfb, D, out_dtype == FP8_OUT_BF16, ldd, status,
-                       as_stream(stream));
+    return launch_gemm(M, N, K, A, lda, fa, ga, sfa, B, ldb, fb, gb, sfb, D, out_dtype == FP8_OUT_BF16 ? 1 : 0, ldd,
+                       nullptr, nullptr, status, as_stream(stream));
+}
+
+fp8_status fp8_scaled_gemm_quantize(fp8_gemm_op op, int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                                    fp8_format fa, const float* sfa, const uint8_t* B, int64_t ldb, fp8_format fb,
+                                    const float* sfb, uint8_t* Dq, int64_t ldd, fp8_format fd, const float* scale_d,
+                                    float* amax_d, int32_t* status, void* stream) {
+    g_detail[0] = 0;
+    FP8_REQUIRE(op == FP8_GEMM_FPROP || op == FP8_GEMM_DGRAD || op == FP8_GEMM_WGRAD, FP8_ERR_INVALID_ARG,
+                "unknown gemm op %d", (int)op);
+    FP8_REQUIRE(M >= 0 && N >= 0 && K >= 0, FP8_ERR_INVALID_ARG, "negative size");
+    FP8_REQUIRE(valid_fmt(fa) && valid_fmt(fb) && valid_fmt(fd), FP8_ERR_INVALID_ARG, "unknown format");
+    FP8_REQUIRE(ldd >= N, FP8_ERR_INVALID_ARG, "ldd < N");
+    if (M == 0 || N == 0) return FP8_OK;
+    FP8_REQUIRE(Dq != nullptr && scale_d != nullptr, FP8_ERR_INVALID_ARG, "Dq or scale_d is NULL");
+    FP8_REQUIRE(aligned(scale_d, 4) && (!amax_d || aligned(amax_d, 4)), FP8_ERR_INVALID_ARG,
+                "scale_d and amax_d must be 4-byte aligned");
+    FP8_REQUIRE(N % 16 == 0 && ldd % 16 == 0, FP8_ERR_UNSUPPORTED, "N and ldd must be multiples of 16");
+    FP8_REQUIRE(aligned(Dq, 16), FP8_ERR_UNSUPPORTED, "Dq must be 16-byte aligned");
+    FP8_REQUIRE(M < (1ll << 31) && N < (1ll << 31) && K < (1ll << 31), FP8_ERR_UNSUPPORTED, "dimension >= 2^31");
+    if (K == 0) {  // D = 0: every code is +0 and max|D| = 0 leaves amax_d as it is
+        cudaError_t e = cudaMemset2DAsync(Dq, (size_t)ldd, 0, (size_t)N, (size_t)M, as_stream(stream));
+        FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaMemset2DAsync: %s", cudaGetErrorString(e));
+        return FP8_OK;
+    }
+    FP8_REQUIRE(A != nullptr && B != nullptr, FP8_ERR_INVALID_ARG, "A or B is NULL");
+    FP8_REQUIRE(sfa != nullptr && sfb != nullptr, FP8_ERR_INVALID_ARG, "sfa and sfb are required");
+    FP8_REQUIRE(lda >= K && ldb >= K, FP8_ERR_INVALID_ARG, "lda/ldb < K");
+    FP8_REQUIRE(K % 16 == 0 && lda % 16 == 0 && ldb % 16 == 0, FP8_ERR_UNSUPPORTED,
+                "K, lda and ldb must be multiples of 16");
+    FP8_REQUIRE(aligned(A, 16) && aligned(B, 16), FP8_ERR_UNSUPPORTED, "A and B must be 16-byte aligned");
+    FP8_REQUIRE(aligned(sfa, 4) && aligned(sfb, 4), FP8_ERR_INVALID_ARG, "sfa/sfb must be 4-byte aligned");
+    return launch_gemm(M, N, K, A, lda, fa, FP8_SCALE_TENSOR, sfa, B, ldb, fb, FP8_SCALE_TENSOR, sfb, Dq,
+                       fd == FP8_E4M3 ? 2 : 3, ldd, scale_d, amax_d, status, as_stream(stream));
 }
 
 }  // extern "C"

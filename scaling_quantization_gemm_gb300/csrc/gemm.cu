@@ -75,6 +75,8 @@ struct GemmArgs {
     int vec_a, vec_b;        // scale rows allow 16-byte loads of four K tiles
     int pair;                // CTA-pair kernel (256-row tiles)
     int32_t* status;
+    const float* sd;  // FP8 output: scale 2^e applied before the cast
+    float* amax_d;    // FP8 output: max |D| before that scale is accumulated here (or NULL)
 };
 
 __device__ __forceinline__ void tile_coords(int t, const GemmArgs& g, int& tm, int& tn) {
@@ -112,6 +114,50 @@ __device__ __forceinline__ void store_row32(const GemmArgs& g, int64_t row, int6
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
+    }
+}
+
+// FP8 output (the next layer's cast fused into this epilogue): 32 values of one row
+// v = (acc sa) sb, code = RNE_sat(v sd), max |v| folded into `amax` (as bits, so a NaN wins).
+template <int FMT>
+__device__ __forceinline__ void store_row32_fp8(const GemmArgs& g, int64_t row, int64_t col0, const uint32_t (&r)[32],
+                                                float sa, float sb, float sd, uint32_t& amax) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (col0 + 16 * h >= g.N) break;
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float v0 = __fmul_rn(__fmul_rn(__uint_as_float(r[16 * h + 2 * i]), sa), sb);
+            const float v1 = __fmul_rn(__fmul_rn(__uint_as_float(r[16 * h + 2 * i + 1]), sa), sb);
+            amax = max(amax, max(__float_as_uint(v0) & 0x7FFFFFFFu, __float_as_uint(v1) & 0x7FFFFFFFu));
+            const uint32_t c = cvt_fp8x2<FMT>(__fmul_rn(v0, sd), __fmul_rn(v1, sd));
+            if (i & 1)
+                w[i >> 1] |= c << 16;
+            else
+                w[i >> 1] = c;
+        }
+        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(g.D) + row * g.ldd + col0 + 16 * h) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Store one accumulator row chunk for output kind OUT: 0 fp32, 1 bf16, 2 E4M3, 3 E5M2.
+template <int OUT>
+__device__ __forceinline__ void store_out(const GemmArgs& g, int64_t row, int64_t col0, const uint32_t (&r)[32],
+                                          float sa, float sb, float sd, uint32_t& amax) {
+    if constexpr (OUT >= 2)
+        store_row32_fp8<OUT - 2>(g, row, col0, r, sa, sb, sd, amax);
+    else
+        store_row32<OUT>(g, row, col0, r, sa, sb);
+}
+
+// End of an epilogue warp: fold the warp's amax into the caller's accumulator.
+template <int OUT>
+__device__ __forceinline__ void flush_amax(const GemmArgs& g, uint32_t amax) {
+    if constexpr (OUT >= 2) {
+        amax = __reduce_max_sync(0xffffffffu, amax);
+        if ((threadIdx.x & 31) == 0 && g.amax_d != nullptr) atomicMax(reinterpret_cast<unsigned int*>(g.amax_d), amax);
     }
 }
 
@@ -178,7 +224,7 @@ struct alignas(1024) SmemPT {
     int abort_flag;
 };
 
-template <int OUT_BF16>
+template <int OUT>
 __global__ void __launch_bounds__(192, 1)
     gemm_tensor_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g,
                        uint32_t idesc) {
@@ -249,6 +295,8 @@ __global__ void __launch_bounds__(192, 1)
     } else {
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const float sa = *g.sa, sb = *g.sb;
+        const float sd = OUT >= 2 ? *g.sd : 1.0f;
+        uint32_t amax = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < g.num_tiles; t += gridDim.x) {
@@ -265,7 +313,7 @@ __global__ void __launch_bounds__(192, 1)
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
                 const int64_t col0 = (int64_t)tn * BN + c * 32;
-                if (row < g.M) store_row32<OUT_BF16>(g, row, col0, r, sa, sb);
+                if (row < g.M) store_out<OUT>(g, row, col0, r, sa, sb, sd, amax);
             }
             tc_fence_before();
             __syncwarp();
@@ -273,6 +321,7 @@ __global__ void __launch_bounds__(192, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
+        flush_amax<OUT>(g, amax);
     }
 
     tc_fence_before();
@@ -304,7 +353,7 @@ struct alignas(1024) SmemPair {
     int abort_flag;
 };
 
-template <int OUT_BF16>
+template <int OUT>
 __global__ void __launch_bounds__(192, 1)
     gemm_tensor_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g,
                             uint32_t idesc) {
@@ -408,6 +457,8 @@ __global__ void __launch_bounds__(192, 1)
     } else {
         const int q = warp & 3;
         const float sa = *g.sa, sb = *g.sb;
+        const float sd = OUT >= 2 ? *g.sd : 1.0f;
+        uint32_t amax = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = cid; t < g.num_tiles; t += ncl) {
@@ -424,7 +475,7 @@ __global__ void __launch_bounds__(192, 1)
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
                 const int64_t col0 = (int64_t)tn * kPairTile + c * 32;
-                if (row < g.M) store_row32<OUT_BF16>(g, row, col0, r, sa, sb);
+                if (row < g.M) store_out<OUT>(g, row, col0, r, sa, sb, sd, amax);
             }
             tc_fence_before();
             __syncwarp();
@@ -432,6 +483,7 @@ __global__ void __launch_bounds__(192, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
+        flush_amax<OUT>(g, amax);
     }
 
     tc_fence_before();
@@ -1086,12 +1138,22 @@ fp8_status launch_pair_kernel(Kernel k, size_t smem, int threads, cudaStream_t s
     return check_launch("CTA-pair GEMM launch");
 }
 
-template <int OUT_BF16>
+template <int OUT>
 fp8_status launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g, uint32_t idesc,
                        cudaStream_t st) {
-    fp8_status s = prepare_kernel(reinterpret_cast<const void*>(gemm_tensor_pair_kernel<OUT_BF16>), sizeof(SmemPair) + 1024);
+    fp8_status s = prepare_kernel(reinterpret_cast<const void*>(gemm_tensor_pair_kernel<OUT>), sizeof(SmemPair) + 1024);
     if (s != FP8_OK) return s;
-    return launch_pair_kernel(gemm_tensor_pair_kernel<OUT_BF16>, sizeof(SmemPair) + 1024, 192, st, tmA, tmB, g, idesc);
+    return launch_pair_kernel(gemm_tensor_pair_kernel<OUT>, sizeof(SmemPair) + 1024, 192, st, tmA, tmB, g, idesc);
+}
+
+template <int OUT>
+fp8_status launch_single(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g, uint32_t idesc, int grid,
+                         cudaStream_t st) {
+    const size_t smem = sizeof(SmemPT) + 1024;
+    fp8_status s = prepare_kernel(reinterpret_cast<const void*>(gemm_tensor_kernel<OUT>), smem);
+    if (s != FP8_OK) return s;
+    gemm_tensor_kernel<OUT><<<grid, 192, smem, st>>>(tmA, tmB, g, idesc);
+    return check_launch("gemm_tensor_kernel launch");
 }
 
 int sf_kind(int gran) { return gran == FP8_SCALE_MX_1x32 ? SF_MX : gran == FP8_SCALE_BLOCK_1x128 ? SF_ROW : SF_BLOCK; }
@@ -1139,9 +1201,11 @@ fp8_status dispatch_bs(int ka, int kb, const CUtensorMap& tmA, const CUtensorMap
 
 }  // namespace
 
+// out: 0 fp32, 1 bf16, 2 E4M3, 3 E5M2 (the FP8 outputs take the per-tensor path only, with sd / amax_d).
 fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, int fa, int ga, const void* sfa,
-                       const uint8_t* B, int64_t ldb, int fb, int gb, const void* sfb, void* D, int out_bf16,
-                       int64_t ldd, int32_t* status, cudaStream_t st) {
+                       const uint8_t* B, int64_t ldb, int fb, int gb, const void* sfb, void* D, int out,
+                       int64_t ldd, const float* sd, float* amax_d, int32_t* status, cudaStream_t st) {
+    const int out_bf16 = out == 1;
     const bool blockscaled = ga != FP8_SCALE_TENSOR;
     // two-SM tiles once the second half of a 256-row tile has work; block-scaled pairs TMA-load 16-byte
     // scale rows, which needs K % 512 == 0 and 16-byte aligned scale tensors
@@ -1164,6 +1228,8 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
     g.sfa = g.sfb = nullptr;
     g.sfa_ld = g.sfb_ld = 0;
     g.vec_a = g.vec_b = 0;
+    g.sd = sd;
+    g.amax_d = amax_d;
 
     CUtensorMap tmA, tmB;
     fp8_status s = make_operand_map(&tmA, A, M, K, lda, BM);
@@ -1175,7 +1241,12 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
         g.sa = static_cast<const float*>(sfa);
         g.sb = static_cast<const float*>(sfb);
         const uint32_t idesc = idesc_f8f6f4(fa, fb, kPairTile, BN);
-        return out_bf16 ? launch_pair<1>(tmA, tmB, g, idesc, st) : launch_pair<0>(tmA, tmB, g, idesc, st);
+        switch (out) {
+            case 0: return launch_pair<0>(tmA, tmB, g, idesc, st);
+            case 1: return launch_pair<1>(tmA, tmB, g, idesc, st);
+            case 2: return launch_pair<2>(tmA, tmB, g, idesc, st);
+            default: return launch_pair<3>(tmA, tmB, g, idesc, st);
+        }
     }
 
     const int grid = std::min(g.num_tiles, device_sm_count());
@@ -1183,15 +1254,12 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
         g.sa = static_cast<const float*>(sfa);
         g.sb = static_cast<const float*>(sfb);
         const uint32_t idesc = idesc_f8f6f4(fa, fb, BM, BN);
-        const size_t smem = sizeof(SmemPT) + 1024;
-        if (out_bf16) {
-            if ((s = prepare_kernel(reinterpret_cast<const void*>(gemm_tensor_kernel<1>), smem)) != FP8_OK) return s;
-            gemm_tensor_kernel<1><<<grid, 192, smem, st>>>(tmA, tmB, g, idesc);
-        } else {
-            if ((s = prepare_kernel(reinterpret_cast<const void*>(gemm_tensor_kernel<0>), smem)) != FP8_OK) return s;
-            gemm_tensor_kernel<0><<<grid, 192, smem, st>>>(tmA, tmB, g, idesc);
+        switch (out) {
+            case 0: return launch_single<0>(tmA, tmB, g, idesc, grid, st);
+            case 1: return launch_single<1>(tmA, tmB, g, idesc, grid, st);
+            case 2: return launch_single<2>(tmA, tmB, g, idesc, grid, st);
+            default: return launch_single<3>(tmA, tmB, g, idesc, grid, st);
         }
-        return check_launch("gemm_tensor_kernel launch");
     }
     g.sfa = sfa;
     g.sfb = sfb;

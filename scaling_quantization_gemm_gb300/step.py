@@ -18,6 +18,16 @@ buffers are torch tensors; torch is only the allocator.
   uses current scaling (the fused amax + scale + cast).
 * ``BlockLinearFwd`` is the forward with per-block (1x128 activations,
   128x128 weights) or MXFP8 (1x32, E8M0) scales.
+* ``bias_sweep`` casts a tensor at a range of fixed (FP8-CSCALE) biases and
+  reports, per bias, how many elements saturate and how many flush to zero
+  ("Training and inference of large language models using 8-bit floating
+  point", "Key findings": the fixed-scaling sweep).
+* ``PTQStack`` is post-training-quantised inference through two FP8 linear
+  layers: weights cast once, the input cast per forward (current or delayed
+  scaling), the hidden activation cast in the first GEMM's epilogue with its
+  delayed scale ("Training and inference of large language models using 8-bit
+  floating point", "Proposed method": inference with post-training
+  quantization, scaling before and unscaling after each FP8 product).
 """
 from __future__ import annotations
 
@@ -27,8 +37,8 @@ from typing import Optional
 import torch
 
 from . import (BLOCK_1x128, BLOCK_128x128, DGRAD, E4M3, E5M2, FPROP, MX_1x32, TENSOR, WGRAD, current_workspace,
-               fp8_amax, fp8_amax_history_update, fp8_compute_scale, fp8_quantize, fp8_quantize_current,
-               fp8_scaled_gemm)
+               fp8_amax, fp8_amax_history_update, fp8_cast_stats, fp8_compute_scale, fp8_quantize,
+               fp8_quantize_current, fp8_scaled_gemm, fp8_scaled_gemm_quantize, fp8_set_bias)
 
 
 class ScaleState:
@@ -62,6 +72,26 @@ def quantize_current(x: torch.Tensor, st: ScaleState, ws: torch.Tensor, q_row=No
     """Current scaling and the cast in one launch: st.amax = max|x|, st.bias/scale/scale_inv from it."""
     fp8_quantize_current(x, st.fmt, st.margin, ws, q_row=q_row, q_col=q_col, amax=st.amax, bias=st.bias,
                          scale=st.scale, scale_inv=st.scale_inv, status=st.status)
+
+
+def bias_sweep(x: torch.Tensor, fmt: int, biases=range(-3, 4)) -> list:
+    """Fixed biases e (FP8-CSCALE) on tensor x: one pass over x per 8 biases.  Returns, per e, the
+    number and fraction of elements the cast saturates and flushes to zero."""
+    biases = list(biases)
+    dev = x.device
+    out = []
+    for i in range(0, len(biases), 8):
+        chunk = biases[i:i + 8]
+        scales = torch.empty(len(chunk), dtype=torch.float32, device=dev)
+        for j, e in enumerate(chunk):
+            fp8_set_bias(e, scale=scales[j:j + 1])
+        sat = torch.zeros(len(chunk), dtype=torch.int64, device=dev)
+        und = torch.zeros(len(chunk), dtype=torch.int64, device=dev)
+        fp8_cast_stats(x, fmt, scales, sat, und)
+        for e, s_, u in zip(chunk, sat.tolist(), und.tolist()):
+            out.append({"e": e, "saturated": s_, "underflow": u, "saturated_frac": s_ / max(x.numel(), 1),
+                        "underflow_frac": u / max(x.numel(), 1)})
+    return out
 
 
 def gemm_flops(m: int, n: int, k: int) -> float:
@@ -204,6 +234,61 @@ class BlockLinearFwd:
     def run(self) -> None:
         self.quantize()
         self.gemm()
+
+
+class PTQStack:
+    """Inference through two FP8 linear layers with post-training quantisation.
+
+    W1 [F x H] and W2 [H x F] are cast to E4M3 once, with current scaling, when the stack is
+    built.  Each forward on X [T x H]:
+      QX = cast(X)                      current scaling (fused kernel), or delayed (`act="delayed"`)
+      QH = cast(unscale(QX . QW1^T))    in GEMM 1's epilogue, with the hidden activation's delayed
+                                        scale; its amax is folded in and recorded afterwards
+      Y  = unscale(QH . QW2^T)          bf16 [T x H]
+    The first forward has no hidden history: GEMM 1 writes bf16 and the hidden activation is cast
+    from its own amax (current scaling); later forwards use the fused epilogue.  No nonlinearity
+    sits between the layers (the method concerns the linear layers only)."""
+
+    def __init__(self, W1: torch.Tensor, W2: torch.Tensor, tokens: int, act: str = "current",
+                 history_len: int = 16):
+        dev = W1.device
+        F, H = W1.shape
+        assert W2.shape == (H, F) and act in ("current", "delayed")
+        self.act, self.T, self.H, self.F = act, tokens, H, F
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.ws = current_workspace(dev)
+        self.sw1, self.sw2 = ScaleState(E4M3, 0, device=dev), ScaleState(E4M3, 0, device=dev)
+        self.qw1, self.qw2 = torch.empty(F, H, **u8), torch.empty(H, F, **u8)
+        quantize_current(W1, self.sw1, self.ws, q_row=self.qw1)  # once: post-training quantisation
+        quantize_current(W2, self.sw2, self.ws, q_row=self.qw2)
+        self.sx = ScaleState(E4M3, 0, history_len if act == "delayed" else 0, dev)
+        self.sh = ScaleState(E4M3, 0, history_len, dev)
+        self.qx, self.qh = torch.empty(tokens, H, **u8), torch.empty(tokens, F, **u8)
+        self.h_bf16: Optional[torch.Tensor] = None  # first forward only
+        self.Y = torch.empty(tokens, H, dtype=torch.bfloat16, device=dev)
+        self.flops = gemm_flops(tokens, F, H) + gemm_flops(tokens, H, F)
+
+    def forward(self, X: torch.Tensor) -> torch.Tensor:
+        sx, sh = self.sx, self.sh
+        if self.act == "current" or sx.steps == 0:
+            quantize_current(X, sx, self.ws, q_row=self.qx)
+        else:
+            fp8_quantize(X, E4M3, TENSOR, scale=sx.scale, q_row=self.qx, amax=sx.amax)
+        if sh.steps == 0:
+            if self.h_bf16 is None:
+                self.h_bf16 = torch.empty(self.T, self.F, dtype=torch.bfloat16, device=X.device)
+            fp8_scaled_gemm(FPROP, self.qx, E4M3, TENSOR, sx.scale_inv, self.qw1, E4M3, TENSOR, self.sw1.scale_inv,
+                            self.h_bf16)
+            quantize_current(self.h_bf16, sh, self.ws, q_row=self.qh)
+        else:
+            fp8_scaled_gemm_quantize(FPROP, self.qx, E4M3, sx.scale_inv, self.qw1, E4M3, self.sw1.scale_inv, self.qh,
+                                     E4M3, sh.scale, sh.amax, status=sh.status)
+        fp8_scaled_gemm(FPROP, self.qh, E4M3, TENSOR, sh.scale_inv, self.qw2, E4M3, TENSOR, self.sw2.scale_inv,
+                        self.Y)
+        sh.advance()
+        if self.act == "delayed":
+            sx.advance()
+        return self.Y
 
 
 def _scale_bytes(rows: int, cols: int, gran: int) -> int:

@@ -148,3 +148,33 @@ def test_quantize_current_noalloc_validation(L):
     assert qn(*a(ld=16)) == 1
     assert qn(*a(cols=12, ld=12)) == 2
     assert qn(*a(rows=24, q_col=FAKE)) == 2
+
+
+def test_gemm_quantize_validation(L):
+    g = L.fp8_scaled_gemm_quantize
+    args = lambda **kw: [kw.get("op", 0), kw.get("M", 128), kw.get("N", 256), kw.get("K", 128), FAKE,
+                         kw.get("lda", 128), 0, FAKE, FAKE, kw.get("ldb", 128), 0, FAKE, kw.get("Dq", FAKE),
+                         kw.get("ldd", 256), kw.get("fd", 0), kw.get("sd", FAKE), None, None, None]
+    assert g(*args(op=4)) == 1
+    assert g(*args(fd=5)) == 1
+    assert g(*args(sd=None)) == 1
+    assert g(*args(Dq=None)) == 1
+    assert g(*args(ldd=200)) == 1  # ldd < N
+    assert g(*args(N=200, ldd=256)) == 2  # N % 16
+    assert g(*args(Dq=FAKE + 8)) == 2  # Dq alignment
+    assert g(*args(K=120, lda=128, ldb=128)) == 2
+    assert g(*args(M=0)) == 0
+
+
+def test_set_bias_and_cast_stats_validation(L):
+    assert L.fp8_set_bias(128, FAKE, FAKE, FAKE, None) == 1
+    assert L.fp8_set_bias(-127, FAKE, FAKE, FAKE, None) == 1
+    assert L.fp8_set_bias(0, None, None, None, None) == 1
+    cs = L.fp8_cast_stats
+    assert cs(FAKE, 32, 32, 32, 0, FAKE, 0, FAKE, FAKE, None) == 1  # n = 0
+    assert cs(FAKE, 32, 32, 32, 0, FAKE, 9, FAKE, FAKE, None) == 1  # n > 8
+    assert cs(FAKE, 32, 32, 32, 2, FAKE, 1, FAKE, FAKE, None) == 1  # format
+    assert cs(FAKE, 32, 32, 32, 0, FAKE, 1, None, FAKE, None) == 1
+    assert cs(FAKE, 32, 32, 32, 0, FAKE, 1, FAKE + 4, FAKE, None) == 1  # counters 8-byte aligned
+    assert cs(FAKE, 32, 12, 12, 0, FAKE, 1, FAKE, FAKE, None) == 2  # cols % 8
+    assert cs(FAKE, 0, 32, 32, 0, FAKE, 1, FAKE, FAKE, None) == 0  # empty

@@ -46,7 +46,8 @@ def test_linear_fwd_current_scaling(q):
 
 def test_delayed_scaling_16_iterations(q):
     """Activation 4096x4096 N(0,1)(1+0.1t), E4M3 margin 0; gradient Laplace(0,1e-4), E5M2 margin 1;
-    history 16.  Iteration 0 scales from its own amax (empty history)."""
+    history 16.  Iteration 0 scales from its own amax (empty history).  Codes, amax, history and
+    the per-iteration saturated / flushed-to-zero counts are exact."""
     from scaling_quantization_gemm_gb300.step import ScaleState, current_scaling
     L = 16
     sa, sg = ScaleState(0, 0, L), ScaleState(1, 1, L)
@@ -57,10 +58,14 @@ def test_delayed_scaling_16_iterations(q):
     for t in range(16):
         xa, xg = wl.delayed_activation(t), wl.delayed_gradient(t)
         da, dg = dev_bf16(xa), dev_bf16(xg)
+        saturated, underflow = {}, {}
         for d, st, out in ((da, sa, qa), (dg, sg, qg)):
             if t == 0:
                 current_scaling(d, st)
             q.fp8_quantize(d, st.fmt, q.TENSOR, scale=st.scale, q_row=out, amax=st.amax)
+            cnt = torch.zeros(2, dtype=torch.int64, device="cuda")
+            q.fp8_cast_stats(d, st.fmt, st.scale, cnt[0:1], cnt[1:2])
+            saturated[st.fmt], underflow[st.fmt] = (int(v) for v in host(cnt))
         got_amax = (host(sa.amax)[0], host(sg.amax)[0])
         ga, gg = host(qa), host(qg)
         for x, st, ref, g, fmt, margin, am in ((xa, sa, ra, ga, 0, 0, got_amax[0]),
@@ -70,6 +75,9 @@ def test_delayed_scaling_16_iterations(q):
             scale = oracle.scale_triple(amax, fmt, margin)[1] if t == 0 else ref.scale[0]
             codes, _ = oracle.quantize_tensor(x, fmt, scale)
             assert_codes_equal(g, codes, fmt, f"iteration {t}")
+            # saturated and flushed counts of this iteration's cast, exact
+            sat_ref, und_ref = oracle.cast_stats(x, fmt, [scale])
+            assert (saturated[fmt], underflow[fmt]) == (int(sat_ref[0]), int(und_ref[0])), t
             ref.update(float(amax), fmt, margin)
             st.advance()
             assert host(st.bias)[0] == ref.bias[0] and host(st.scale)[0] == ref.scale[0]

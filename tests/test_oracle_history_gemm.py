@@ -160,3 +160,60 @@ def test_gemm_tolerance_helper(oracle):
     tb = oracle.gemm_tolerance(y_ref, mag, out_bf16=True)
     # bf16 ulp of 1.0 is 2^-7, of 3.0 is 2^-6, of 1000 is 4
     assert np.allclose(tb - t, [2 ** -8, 2 ** -7, 2.0, 0.0])
+
+
+# ------------------------------------------------ FP8-output bracket
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_gemm_quantize_bracket_brute_force(oracle, fmt):
+    """Every fp32 v in a narrow interval around y is walked one ulp at a time: every
+    Encode(fl32(v s)) lies between the bracket's ends (by value).  Half the y sit exactly on a
+    rounding midpoint (after scaling), where both neighbouring codes must be admitted."""
+    rng = np.random.default_rng(40 + fmt)
+    s = np.float32(2.0 ** 3)
+    fmax = 448.0 if fmt == 0 else 57344.0
+    ys = list(rng.uniform(fmax / 64, fmax / 8, 30) * rng.choice([-1, 1], 30))
+    for c in rng.integers(1, 0x7E if fmt == 0 else 0x7B, 30):  # midpoints between code c and c+1
+        mid = (oracle.decode(int(c), fmt) + oracle.decode(int(c) + 1, fmt)) / 2
+        ys.append(mid / float(s))
+    for k, y in enumerate(ys):
+        tol = abs(y) * 2e-6
+        lo, hi, near = oracle.gemm_quantize_bracket(np.array([y]), np.array([tol]), fmt, s)
+        dlo, dhi = oracle.decode(int(lo[0]), fmt), oracle.decode(int(hi[0]), fmt)
+        assert dlo <= oracle.decode(int(near[0]), fmt) <= dhi
+        v = np.float32(y - tol)
+        seen = set()
+        while float(v) <= y + tol:
+            if float(v) >= y - tol:
+                d = oracle.decode(oracle.encode(float(np.float32(v * s)), fmt), fmt)
+                assert dlo <= d <= dhi, (y, float(v), d)
+                seen.add(d)
+            v = np.nextafter(v, np.float32(np.inf))
+        assert seen <= {dlo, dhi}
+        if k >= 30:  # on a midpoint: both neighbours are reachable and admitted
+            assert seen == {dlo, dhi} and dlo < dhi
+
+
+def test_gemm_quantize_bracket_exact_values(oracle):
+    """tol = 0 on values exactly representable after scaling: lo = hi = the code of y s."""
+    for fmt in (0, 1):
+        codes = np.array([c for c in range(256) if not np.isnan(oracle.decode(c, fmt))], np.uint8)
+        y = oracle.decode_array(codes, fmt) / 4.0  # scale 4 maps y back onto the codes
+        lo, hi, near = oracle.gemm_quantize_bracket(y, np.zeros_like(y), fmt, 4.0)
+        keep = np.abs(y * 4) < (448 if fmt == 0 else 57344) + 1  # Inf codes of E5M2 saturate
+        assert np.array_equal(lo[keep] & 0x7F, codes[keep] & 0x7F)
+        # by value: -0 - 0 and -0 + 0 differ in sign only
+        dl, dh, dn = (oracle.decode_array(c, fmt) for c in (lo, hi, near))
+        assert np.array_equal(dl, dh) and np.array_equal(dn, dl)
+
+
+def test_round_bf16_matches_torch(oracle):
+    """bf16 rounding (ties to even) against torch's CPU float32 -> bfloat16 conversion."""
+    import torch
+    rng = np.random.default_rng(77)
+    v = np.concatenate([rng.standard_normal(20000).astype(np.float32) * np.float32(1e3),
+                        np.exp2(rng.uniform(-130, 120, 20000)).astype(np.float32),
+                        # exact ties: bf16 value plus half a bf16 ulp
+                        (np.arange(1, 5000, dtype=np.uint32) << 16 | 0x8000).view(np.float32)])
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(oracle.round_bf16(v).view(np.uint32), ref.view(np.uint32))

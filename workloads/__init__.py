@@ -124,6 +124,15 @@ def ffn_fwd_bwd(m: int = 16384, k: int = 5120, n: int = 20480):
 
 # ---------------------------------------------------------- test helpers
 
+def ptq_ffn(t: int = 8192, h: int = 5120, f: int = 13824, seed: int = 0):
+    """Inference through a 13B-class FFN (hidden 5120, intermediate 13824): X [t x h] N(0,1),
+    W1 [f x h] and W2 [h x f] N(0, 0.02^2); seeds seed, seed+1, seed+2."""
+    X = normal(np.random.default_rng(seed), t, h, 1.0)
+    W1 = normal(np.random.default_rng(seed + 1), f, h, 0.02)
+    W2 = normal(np.random.default_rng(seed + 2), h, f, 0.02)
+    return X, W1, W2
+
+
 def random_bf16(seed: int, rows: int, cols: int, kind: str = "normal", scale: float = 1.0) -> np.ndarray:
     """Small seeded bf16 matrices for parity tests of odd shapes.
     kind: normal | laplace | t3 | wide (log-uniform magnitudes over ~2^-40..2^40) | zeros."""
