@@ -9,12 +9,13 @@
 // Effective FP8 Training", "Key Questions Answered").
 //
 // All of it is HBM-bound.  The cast kernel streams 128x128 bf16 tiles through
-// a three-deep TMA ring in shared memory (loads for the next two tiles are in
-// flight while one is processed), computes block maxima in registers (warp
-// shuffles), writes the row-wise codes, and reads the same tile down its
-// columns for the transposed column-wise codes, so one HBM read feeds both
-// outputs.  The fused amax is reduced per warp, per CTA, then one atomic per
-// CTA.
+// a two-deep TMA ring per CTA, three CTAs per SM (up to six tile loads in
+// flight per SM), computes block maxima in registers (warp shuffles), writes
+// the row-wise codes, and reads the same tile down its columns for the
+// transposed column-wise codes, so one HBM read feeds both outputs.  The fused
+// amax is reduced per warp, per CTA, then one atomic per CTA.  Current scaling
+// runs the amax pass and the cast in one cooperative launch with a grid
+// barrier between them.
 #include <cudaTypedefs.h>
 
 #include <cstdarg>
