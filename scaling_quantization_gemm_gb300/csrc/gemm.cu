@@ -745,17 +745,24 @@ __global__ void __launch_bounds__(320, 1)
 
 // A pair computes a 256x224 tile with tcgen05.mma.cta_group::2 ... block_scale:
 // each CTA holds 128 rows of A and 112 rows of B per K tile (30 KB per stage,
-// 4 stages) and 128 rows of the accumulator.  Each CTA's tensor core reads the
+// 6 stages) and 128 rows of the accumulator.  Each CTA's tensor core reads the
 // scales of its own A rows and of all 224 B rows from its own TMEM, so both
 // CTAs' scale writers fill their own scale slots (A row m: lane m, column m/32;
 // B row n: lane 32q + n%32, column 8 + n/32, every quarter q).  The producer
 // TMA-loads the scales of each group of four K tiles (16 bytes per row: the A
 // rows of this CTA and all B rows of the tile) into a four-slot shared-memory
-// ring, two groups ahead; the writers read them there.  The even CTA's `full`
-// barrier of a stage completes when both producers' loads have landed and all
-// eight scale writers of the pair have written that stage's scale slot, so the
-// producers never wait for the writers.
-constexpr int kBsPairStages = 4;
+// ring, two groups ahead; the writers read them there.  TMEM has room for four
+// scale slots (64 columns beside the two 224-column accumulators), fewer than
+// the six operand stages: K tile i (counted over all of a pair's tiles) uses
+// stage i % 6 and scale slot i % 4.  The even CTA's `full[stage]` completes
+// when both producers' loads have landed and all eight scale writers of the
+// pair have written the slot, so the issuing thread waits once and commits
+// once per K tile.  A writer may overwrite slot i % 4 once the MMAs of K tile
+// i - 4, its last reader, are done, which is completion (i - 4) / 6 of
+// `empty[(i - 4) % 6]`; that barrier cannot run a completion further ahead,
+// because the MMAs of K tile i + 2 wait for the writers of K tile i + 2.
+constexpr int kBsPairStages = 6;
+constexpr int kSfSlots = 4;  // TMEM scale slots (kSfColsPerStage columns each)
 constexpr int kBsPairB = BN_BS / 2;                    // 112 rows of B per CTA
 constexpr int kBsPairABytes = kPairRows * BK;          // 16 KB
 constexpr int kBsPairBBytes = kBsPairB * BK;           // 14 KB
@@ -896,7 +903,7 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
-            int stage = 0, acc = 0;
+            int stage = 0, acc = 0, slot = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int t = cid; ok && t < g.num_tiles; t += ncl) {
@@ -911,7 +918,7 @@ __global__ void __launch_bounds__(320, 1)
                     tc_fence_after();
                     const uint64_t ad = sdesc_kmajor_sw128(smem_u32(S.a[stage]));
                     const uint64_t bd = sdesc_kmajor_sw128(smem_u32(S.b[stage]));
-                    const uint32_t sfa_t = tmem + (uint32_t)(kSfColBase + stage * kSfColsPerStage);
+                    const uint32_t sfa_t = tmem + (uint32_t)(kSfColBase + slot * kSfColsPerStage);
                     const uint32_t sfb_t = sfa_t + 8;
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
@@ -922,6 +929,7 @@ __global__ void __launch_bounds__(320, 1)
                         stage = 0;
                         phase ^= 1;
                     }
+                    if (++slot == kSfSlots) slot = 0;
                 }
                 if (!ok) break;
                 tc_commit_pair_multicast(smem_u32(&S.tfull[acc]), 0x3);
@@ -965,8 +973,7 @@ __global__ void __launch_bounds__(320, 1)
         // read from the shared-memory scale ring.
         const int q = warp & 3;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        int stage = 0;
-        uint32_t phase = 0;
+        int kcount = 0;  // K tiles written so far (over all of this pair's tiles)
         int consumed = 0;
         uint32_t bad = 0;
         bool ok = true;
@@ -986,13 +993,19 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     if (4 * grp + jj >= g.k_tiles) break;
-                    w = mbar_wait_bounded(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag);
-                    if (!__all_sync(0xffffffffu, w)) {
-                        ok = false;
-                        break;
+                    if (kcount >= kSfSlots) {  // the MMAs of K tile kcount - 4 are done with this slot
+                        const int prev = kcount - kSfSlots;
+                        w = mbar_wait_bounded(smem_u32(&S.empty[prev % kBsPairStages]),
+                                              (uint32_t)((prev / kBsPairStages) & 1), abort_flag);
+                        if (!__all_sync(0xffffffffu, w)) {
+                            ok = false;
+                            break;
+                        }
                     }
                     tc_fence_after();
-                    const uint32_t tslot = tmem + lane_base + (uint32_t)(kSfColBase + stage * kSfColsPerStage);
+                    const int stage = kcount % kBsPairStages;
+                    const uint32_t tslot =
+                        tmem + lane_base + (uint32_t)(kSfColBase + (kcount % kSfSlots) * kSfColsPerStage);
                     tmem_st_32x32b_x1(tslot + q, sf_word_smem<KA>(S.sa[slot], q * 32 + lane, jj, ablock, arow, g.M, bad));
                     uint32_t wb[8];
 #pragma unroll
@@ -1005,10 +1018,7 @@ __global__ void __launch_bounds__(320, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&S.full[stage]), 0));
-                    if (++stage == kBsPairStages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
+                    ++kcount;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.scale_empty[slot]));
