@@ -52,6 +52,7 @@ struct alignas(1024) QuantSmem {
     uint64_t empty[kQStages];  // one arrival per warp when it is done with the stage
     uint32_t red[2][8];
     uint32_t col_part[4][64];
+    uint32_t col_sf[2][128];  // MX column scales of a tile: four 32-row segments (bytes) per column
     uint32_t am[8];
     int abort_flag;
 };
@@ -167,8 +168,9 @@ __device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const Qua
     const int rsub = tid >> 4;
     const int64_t n_my = (a.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
 
-    // tiles that need a block-wide reduction keep the CTA in lock step
-    const bool lockstep = GRAN == FP8_SCALE_BLOCK_128x128 || (GRAN == FP8_SCALE_BLOCK_1x128 && a.do_col);
+    // tiles that need a block-wide reduction keep the CTA in lock step (MX column scales: the four
+    // 32-row segments of a column come from four warps and leave as one 4-byte store)
+    const bool lockstep = GRAN == FP8_SCALE_BLOCK_128x128 || ((GRAN == FP8_SCALE_BLOCK_1x128 || GRAN == FP8_SCALE_MX_1x32) && a.do_col);
     if (tid == 0) {
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(smem_u32(&S.full[s]), 1);
@@ -321,11 +323,22 @@ __device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const Qua
                 const int eB = bias_bf16(mm >> 16, FMT, a.margin);
                 sA = pow2_bf16x2(eA);
                 sB = pow2_bf16x2(eB);
-                if (row0 < a.rows) {
-                    uint8_t* sf = static_cast<uint8_t*>(a.sf_col);
+                uint8_t* cs = reinterpret_cast<uint8_t*>(S.col_sf[parity]);
+                cs[4 * (2 * cp) + seg] = (uint8_t)(127 - eA);
+                cs[4 * (2 * cp + 1) + seg] = (uint8_t)(127 - eB);
+                __syncthreads();
+                if (tid < kTile) {  // column c0 + tid: its four segment scales, rows r0 .. r0 + 127
+                    const int64_t c = c0 + tid;
                     const int64_t nb = cdiv(a.rows, 32);
-                    if (ca < a.cols) sf[ca * nb + (row0 >> 5)] = (uint8_t)(127 - eA);
-                    if (cb < a.cols) sf[cb * nb + (row0 >> 5)] = (uint8_t)(127 - eB);
+                    uint8_t* sf = static_cast<uint8_t*>(a.sf_col) + c * nb + (r0 >> 5);
+                    const uint32_t word = S.col_sf[parity][tid];
+                    if (c < a.cols) {
+                        if (r0 + kTile <= a.rows && ((reinterpret_cast<uintptr_t>(sf) & 3) == 0)) {
+                            *reinterpret_cast<uint32_t*>(sf) = word;
+                        } else {
+                            for (int q = 0; q < 4 && r0 + 32 * q < a.rows; ++q) sf[q] = (uint8_t)(word >> (8 * q));
+                        }
+                    }
                 }
             } else {  // 1x128 -> 128x1 column blocks: combine the four 32-row segments
                 S.col_part[seg][cp] = mm;
