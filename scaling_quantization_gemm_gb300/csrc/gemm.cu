@@ -744,36 +744,39 @@ __global__ void __launch_bounds__(320, 1)
 // ================================================== block-scaled GEMM, CTA pair
 
 // A pair computes a 256x224 tile with tcgen05.mma.cta_group::2 ... block_scale:
-// each CTA holds 128 rows of A and 112 rows of B per K tile (30 KB per stage,
-// 6 stages) and 128 rows of the accumulator.  Each CTA's tensor core reads the
+// each CTA holds 128 rows of A and 112 rows of B per 128-wide K tile, two K
+// tiles per stage (60 KB, 3 stages), and 128 rows of the accumulator.  Each CTA's tensor core reads the
 // scales of its own A rows and of all 224 B rows from its own TMEM, so both
 // CTAs' scale writers fill their own scale slots (A row m: lane m, column m/32;
 // B row n: lane 32q + n%32, column 8 + n/32, every quarter q).  The producer
 // TMA-loads the scales of each group of four K tiles (16 bytes per row: the A
 // rows of this CTA and all B rows of the tile) into a four-slot shared-memory
 // ring, two groups ahead; the writers read them there.  TMEM has room for four
-// scale slots (64 columns beside the two 224-column accumulators), fewer than
-// the six operand stages: K tile i (counted over all of a pair's tiles) uses
-// stage i % 6 and scale slot i % 4.  The even CTA's `full[stage]` completes
-// when both producers' loads have landed and all eight scale writers of the
-// pair have written the slot, so the issuing thread waits once and commits
-// once per K tile.  A writer may overwrite slot i % 4 once the MMAs of K tile
-// i - 4, its last reader, are done, which is completion (i - 4) / 6 of
-// `empty[(i - 4) % 6]`; that barrier cannot run a completion further ahead,
-// because the MMAs of K tile i + 2 wait for the writers of K tile i + 2.
-constexpr int kBsPairStages = 6;
+// scale slots (64 columns beside the two 224-column accumulators): K tile i
+// (counted over all of a pair's tiles) uses stage i / 2 % 3 and scale slot
+// i % 4.  The even CTA's `full[stage]` completes when both producers' loads
+// have landed and all eight scale writers of the pair have written the slots
+// of both K tiles, so the issuing thread waits once and commits once per two K
+// tiles (its per-K-tile waits and commits, not the tensor core, set the pace
+// with one K tile per stage).  A writer may overwrite slot i % 4 once the MMAs
+// of K tile i - 4, its last reader, are done, which is completion s / 3 of
+// `empty[s % 3]`, s = (i - 4) / 2; that barrier cannot run a completion
+// further ahead, because the MMAs of stage s + 3 wait for the writers of K
+// tiles past i.
+constexpr int kBsKPerStage = 2;  // 128-wide K tiles per operand stage
+constexpr int kBsPairStages = 3;
 constexpr int kSfSlots = 4;  // TMEM scale slots (kSfColsPerStage columns each)
 constexpr int kBsPairB = BN_BS / 2;                    // 112 rows of B per CTA
-constexpr int kBsPairABytes = kPairRows * BK;          // 16 KB
-constexpr int kBsPairBBytes = kBsPairB * BK;           // 14 KB
-constexpr int kBsPairStageBytes = kBsPairABytes + kBsPairBBytes;
+constexpr int kBsPairABytes = kPairRows * BK;          // 16 KB per K tile
+constexpr int kBsPairBBytes = kBsPairB * BK;           // 14 KB per K tile
+constexpr int kBsPairStageBytes = kBsKPerStage * (kBsPairABytes + kBsPairBBytes);
 constexpr int kScaleSlots = 4;
 constexpr int kScaleAhead = 2;  // scale groups loaded ahead of the group being consumed
 constexpr int kScaleBlockRowsB = 3;                    // 224 B rows touch at most three 128-row blocks
 
 struct alignas(1024) SmemBsPair {
-    uint8_t a[kBsPairStages][kBsPairABytes];
-    uint8_t b[kBsPairStages][kBsPairBBytes];
+    uint8_t a[kBsPairStages][kBsKPerStage * kBsPairABytes];
+    uint8_t b[kBsPairStages][kBsKPerStage * kBsPairBBytes];
     alignas(128) uint8_t sa[kScaleSlots][kPairRows * 16];  // per row: four K tiles x 4 bytes (E8M0 x4 or one fp32)
     alignas(128) uint8_t sb[kScaleSlots][BN_BS * 16];
     uint64_t full[kBsPairStages], empty[kBsPairStages], tfull[2], tempty[2], drain;
@@ -817,7 +820,7 @@ __global__ void __launch_bounds__(320, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBsPairStages; ++s) {
-            mbar_init(smem_u32(&S.full[s]), 2 + 8);  // both producers + the eight scale writers of the pair
+            mbar_init(smem_u32(&S.full[s]), 2 + 8 * kBsKPerStage);  // both producers + 8 writers per K tile
             mbar_init(smem_u32(&S.empty[s]), 1);     // the MMA commit
         }
         for (int s = 0; s < kScaleSlots; ++s) {
@@ -879,15 +882,20 @@ __global__ void __launch_bounds__(320, 1)
             for (int t = cid; ok && t < g.num_tiles; t += ncl) {
                 int tm, tn;
                 tile_coords(t, g, tm, tn);
-                for (int kt = 0; kt < g.k_tiles; ++kt) {
+                for (int kt = 0; kt < g.k_tiles; kt += kBsKPerStage) {  // k_tiles is a multiple of 4 here
                     if ((kt & 3) == 0 && !(ok = issue_next_scales())) break;  // entering a group: keep two ahead
                     if (!mbar_wait_bounded(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
                     const uint32_t full_leader = map_to_cta(smem_u32(&S.full[stage]), 0);
-                    tma_load_2d_pair(smem_u32(S.a[stage]), &tmA, full_leader, kt * BK, tm * kPairTile + (int)rank * kPairRows);
-                    tma_load_2d_pair(smem_u32(S.b[stage]), &tmB, full_leader, kt * BK, tn * BN_BS + (int)rank * kBsPairB);
+#pragma unroll
+                    for (int h = 0; h < kBsKPerStage; ++h) {
+                        tma_load_2d_pair(smem_u32(S.a[stage] + h * kBsPairABytes), &tmA, full_leader, (kt + h) * BK,
+                                         tm * kPairTile + (int)rank * kPairRows);
+                        tma_load_2d_pair(smem_u32(S.b[stage] + h * kBsPairBBytes), &tmB, full_leader, (kt + h) * BK,
+                                         tn * BN_BS + (int)rank * kBsPairB);
+                    }
                     mbar_arrive_expect_tx_cluster(full_leader, kBsPairStageBytes);
                     if (++stage == kBsPairStages) {
                         stage = 0;
@@ -910,26 +918,30 @@ __global__ void __launch_bounds__(320, 1)
                 if (!mbar_wait_bounded(smem_u32(&S.tempty[acc]), acc_phase ^ 1, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * BN_BS);
-                for (int kt = 0; kt < g.k_tiles; ++kt) {
+                for (int kt = 0; kt < g.k_tiles; kt += kBsKPerStage) {
                     if (!mbar_wait_bounded(smem_u32(&S.full[stage]), phase, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_kmajor_sw128(smem_u32(S.a[stage]));
-                    const uint64_t bd = sdesc_kmajor_sw128(smem_u32(S.b[stage]));
-                    const uint32_t sfa_t = tmem + (uint32_t)(kSfColBase + slot * kSfColsPerStage);
-                    const uint32_t sfb_t = sfa_t + 8;
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)
-                        tc_mma_mxf8f6f4_pair(d, ad + 2 * k, bd + 2 * k, idesc | ((uint32_t)k << 29) | ((uint32_t)k << 4),
-                                             sfa_t, sfb_t, (kt | k) != 0 ? 1u : 0u);
+                    for (int h = 0; h < kBsKPerStage; ++h) {
+                        const uint64_t ad = sdesc_kmajor_sw128(smem_u32(S.a[stage] + h * kBsPairABytes));
+                        const uint64_t bd = sdesc_kmajor_sw128(smem_u32(S.b[stage] + h * kBsPairBBytes));
+                        const uint32_t sfa_t = tmem + (uint32_t)(kSfColBase + slot * kSfColsPerStage);
+                        const uint32_t sfb_t = sfa_t + 8;
+#pragma unroll
+                        for (int k = 0; k < BK / 32; ++k)
+                            tc_mma_mxf8f6f4_pair(d, ad + 2 * k, bd + 2 * k,
+                                                 idesc | ((uint32_t)k << 29) | ((uint32_t)k << 4), sfa_t, sfb_t,
+                                                 ((kt + h) | k) != 0 ? 1u : 0u);
+                        if (++slot == kSfSlots) slot = 0;
+                    }
                     tc_commit_pair_multicast(smem_u32(&S.empty[stage]), 0x3);
                     if (++stage == kBsPairStages) {
                         stage = 0;
                         phase ^= 1;
                     }
-                    if (++slot == kSfSlots) slot = 0;
                 }
                 if (!ok) break;
                 tc_commit_pair_multicast(smem_u32(&S.tfull[acc]), 0x3);
@@ -994,7 +1006,7 @@ __global__ void __launch_bounds__(320, 1)
                 for (int jj = 0; jj < 4; ++jj) {
                     if (4 * grp + jj >= g.k_tiles) break;
                     if (kcount >= kSfSlots) {  // the MMAs of K tile kcount - 4 are done with this slot
-                        const int prev = kcount - kSfSlots;
+                        const int prev = (kcount - kSfSlots) / kBsKPerStage;  // the stage step that held it
                         w = mbar_wait_bounded(smem_u32(&S.empty[prev % kBsPairStages]),
                                               (uint32_t)((prev / kBsPairStages) & 1), abort_flag);
                         if (!__all_sync(0xffffffffu, w)) {
@@ -1003,7 +1015,7 @@ __global__ void __launch_bounds__(320, 1)
                         }
                     }
                     tc_fence_after();
-                    const int stage = kcount % kBsPairStages;
+                    const int stage = (kcount / kBsKPerStage) % kBsPairStages;
                     const uint32_t tslot =
                         tmem + lane_base + (uint32_t)(kSfColBase + (kcount % kSfSlots) * kSfColsPerStage);
                     tmem_st_32x32b_x1(tslot + q, sf_word_smem<KA>(S.sa[slot], q * 32 + lane, jj, ablock, arow, g.M, bad));
