@@ -121,19 +121,29 @@ __device__ __forceinline__ uint2 encode8_f32(const uint4& v, float s) {
                       encode2_f32<FMT>(v.z, s) | (encode2_f32<FMT>(v.w, s) << 16));
 }
 
-// Column-wise: the low (HALF = 0) or high (HALF = 1) bf16 of 32 words (32 rows
-// of one column) -> 32 codes in 8 words, row order.
-template <int FMT, int HALF>
-__device__ __forceinline__ void encode_column32(const uint32_t (&w)[32], uint32_t s2, uint32_t (&o)[8]) {
+// Both columns of a word column at once: w[r] holds rows r of columns A (low) and B (high); s2
+// holds the bf16 scales of A (low) and B (high).  One bf16x2 multiply per row scales both
+// columns, then each column's rows 2p, 2p+1 are converted together.
+template <int FMT>
+__device__ __forceinline__ void encode_column_pair32(const uint32_t (&w)[32], uint32_t s2, uint32_t (&oA)[8],
+                                                     uint32_t (&oB)[8]) {
 #pragma unroll
     for (int p = 0; p < 16; ++p) {
-        // rows 2p, 2p+1 of this column as one bf16x2 word
-        const uint32_t pair = HALF ? __byte_perm(w[2 * p], w[2 * p + 1], 0x7632) : __byte_perm(w[2 * p], w[2 * p + 1], 0x5410);
-        const uint32_t c = encode2<FMT>(pair, s2);
-        if (p & 1) o[p >> 1] |= c << 16; else o[p >> 1] = c;
+        const uint32_t a = mul_bf16x2(w[2 * p], s2), b = mul_bf16x2(w[2 * p + 1], s2);
+        const uint32_t cA = cvt_fp8x2<FMT>(__uint_as_float(a << 16), __uint_as_float(b << 16));
+        const uint32_t cB = cvt_fp8x2<FMT>(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u));
+        if (p & 1) {
+            oA[p >> 1] |= cA << 16;
+            oB[p >> 1] |= cB << 16;
+        } else {
+            oA[p >> 1] = cA;
+            oB[p >> 1] = cB;
+        }
     }
 }
 
+// Column-wise with an arbitrary fp32 scale: the low (HALF = 0) or high (HALF = 1) bf16 of 32 words
+// (32 rows of one column) -> 32 codes in 8 words, row order.
 template <int FMT, int HALF>
 __device__ __forceinline__ void encode_column32_f32(const uint32_t (&w)[32], float s, uint32_t (&o)[8]) {
 #pragma unroll
@@ -367,14 +377,10 @@ __device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const Qua
                     store_col32(a.q_col, cb, a.rows, row0, o);
                 }
             } else {
-                if (ca < a.cols) {
-                    encode_column32<FMT, 0>(w, sA, o);
-                    store_col32(a.q_col, ca, a.rows, row0, o);
-                }
-                if (cb < a.cols) {
-                    encode_column32<FMT, 1>(w, sB, o);
-                    store_col32(a.q_col, cb, a.rows, row0, o);
-                }
+                uint32_t oB[8];
+                encode_column_pair32<FMT>(w, (sA & 0xFFFFu) | (sB & 0xFFFF0000u), o, oB);
+                if (ca < a.cols) store_col32(a.q_col, ca, a.rows, row0, o);
+                if (cb < a.cols) store_col32(a.q_col, cb, a.rows, row0, oB);
             }
         }
         __syncwarp();

@@ -237,3 +237,25 @@ def test_quantize_tensor_arbitrary_scale(q, fmt, scale_val):
     rr, rc = oracle.quantize_tensor(x, fmt, np.float32(scale_val), row=True, col=True)
     assert_codes_equal(qr, rr, fmt, "row")
     assert_codes_equal(qc, rc, fmt, "col")
+
+
+def test_calls_run_on_the_callers_stream(q):
+    """Work is enqueued on the caller's (current) stream: each call sees the producer that ran just
+    before it on the same side stream, without any synchronisation with other streams."""
+    xb = wl.random_bf16(61, 4096, 4096, "normal")
+    amax_ref = oracle.amax(xb)
+    base = dev_bf16(xb)
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        x = torch.zeros_like(base)
+        for _ in range(20):  # keep the producer busy for a while
+            x.copy_(base * 1.0)
+        amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+        q.fp8_amax(x, amax)
+        out = torch.empty(4096, 4096, dtype=torch.uint8, device="cuda")
+        scale = torch.tensor([float(oracle.scale_triple(amax_ref, 0)[1])], device="cuda")
+        q.fp8_quantize(x, 0, q.TENSOR, scale=scale, q_row=out)
+    side.synchronize()
+    assert host(amax)[0] == amax_ref
+    assert_codes_equal(host(out), oracle.quantize_tensor(xb, 0, oracle.scale_triple(amax_ref, 0)[1])[0], 0)
