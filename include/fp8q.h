@@ -18,9 +18,10 @@
  *
  * Conventions shared by every entry point:
  *   - Every pointer argument that names a tensor is a DEVICE pointer into memory
- *     the caller allocated and owns.  The library allocates no device memory,
- *     keeps no global state between calls, and is safe to call from several
- *     host threads on different streams.
+ *     the caller allocated and owns.  The library allocates no device memory and
+ *     keeps no state between calls (the one exception is the static scratch of
+ *     fp8_quantize_current_noalloc); it is safe to call from several host
+ *     threads on different streams.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
  *     only enqueues work on that stream and returns; none synchronises the host.
  *   - Arguments are validated on the host before anything is enqueued:
@@ -35,10 +36,10 @@
  *   - bf16 inputs are row-major [rows x cols] with leading dimension `ld`
  *     (elements, ld >= cols).  FP8 outputs are one byte per element, OFP8 E4M3
  *     or E5M2 bit patterns, row-major and dense.
- *   - Scales are powers of two.  A per-tensor quantisation scale is the
- *     multiplier s = 2^e applied before the cast; the GEMM takes the
- *     dequantisation factor s^-1 = 2^-e.  Block scales are stored as
- *     dequantisation factors (fp32 2^-e, or the E8M0 code 127 - e).
+ *   - The scales this library derives are powers of two.  A per-tensor
+ *     quantisation scale is the multiplier s = 2^e applied before the cast; the
+ *     GEMM takes the dequantisation factor s^-1 = 2^-e.  Block scales are stored
+ *     as dequantisation factors (fp32 2^-e, or the E8M0 code 127 - e).
  */
 #ifndef FP8Q_H
 #define FP8Q_H
