@@ -300,7 +300,9 @@ FP8Q_API fp8_status fp8_quantize_current_noalloc(const void *x, int64_t rows, in
  *              otherwise neither may be TENSOR, and each of sfa / sfb is
  *                1x128:   fp32 [rows x ceil(K/128)]
  *                128x128: fp32 [ceil(rows/128) x ceil(K/128)]
- *                MX 1x32: u8 E8M0 [rows x ceil(K/32)] (K must be a multiple of 32)
+ *                MX 1x32: u8 E8M0 [rows x ceil(K/32)] (K must be a multiple of 32;
+ *                  fp8_quantize writes codes 0..253; code 255, NaN in the OCP
+ *                  MX encoding, gives an unspecified result)
  *              (rows = M for A, N for B).  fp32 block scales must be powers of
  *              two in [2^-127, 2^127] (what fp8_quantize writes); any other
  *              value sets FP8_STATUS_BAD_BLOCK_SCALE.

@@ -185,3 +185,22 @@ def test_gemm_bad_block_scale_sets_status(q):
     sfb = pow2_scales(rng, (N // 128 + 1, K // 128))
     _, st = run_gemm(q, A, 0, 1, sfa, B, 0, 2, sfb, True)
     assert st == q.STATUS_BAD_BLOCK_SCALE
+
+
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_gemm_nan_operand_poisons_its_row_only(q, out_bf16):
+    """A NaN code in A makes its output row NaN (the fp64 oracle agrees); every other row is finite
+    and within tolerance."""
+    rng = np.random.default_rng(12)
+    A = realistic_codes(rng, (256, 512), 0)
+    B = realistic_codes(rng, (256, 512), 0)
+    A[3, 10] = 0x7F  # E4M3 NaN
+    sa, sb = np.array([2.0 ** -6], np.float32), np.array([2.0 ** -6], np.float32)
+    y, st = run_gemm(q, A, 0, 0, sa, B, 0, 0, sb, out_bf16)
+    y_ref, mag = oracle.gemm_full(A, 0, 0, sa, B, 0, 0, sb)
+    assert st == 0
+    assert np.isnan(y[3]).all() and np.isnan(y_ref[3]).all()
+    keep = np.ones(256, bool)
+    keep[3] = False
+    assert np.isfinite(y[keep]).all()
+    assert_gemm_close(y[keep], y_ref[keep], mag[keep], out_bf16)
