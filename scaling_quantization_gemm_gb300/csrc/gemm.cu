@@ -6,29 +6,31 @@
 // per-block / MXFP8 scales ("Per-Tensor and Per-Block Scaling Strategies for
 // Effective FP8 Training", "Key Questions Answered").
 //
-// Design (one persistent CTA per SM, warp-specialised):
-//   warp 0      TMA producer: 128x128-byte A tiles and BNx128-byte B tiles,
-//               128-byte swizzle, into a 4-stage shared-memory ring.
+// Design (persistent, warp-specialised, one CTA per SM):
+//   warp 0      TMA producer: A and B tiles (128-byte rows of a 128-wide K
+//               tile, 128-byte swizzle) into a shared-memory ring.
 //   warp 1      allocates TMEM and issues tcgen05.mma (one thread); each
 //               128-wide K tile is four K=32 MMAs.
-//   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), unscale, convert,
-//               store.  Each warp owns the 32 TMEM lanes (= tile rows) that
-//               its warp index selects.
-//   warps 6-9   (block-scaled kernel only) scale-factor writers.
+//   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), unscale, convert
+//               (fp32, bf16, or E4M3/E5M2 with a given scale and a fused amax),
+//               store.  Each warp owns the 32 TMEM lanes (= tile rows) that its
+//               warp index selects.
+//   warps 6-9   (block-scaled kernels only) scale-factor writers.
 // Two fp32 accumulators live in TMEM so the epilogue of one tile overlaps the
-// main loop of the next.
-// Per-tensor: 128x256 tiles (2 x 256 TMEM columns); the unscale
-// 2^-(ea+eb) is applied in the epilogue.
+// main loop of the next.  M > 128 runs on CTA pairs (clusters of two, tcgen05
+// cta_group::2: the even CTA issues the MMAs for both SMs); M <= 128 runs the
+// one-CTA kernels.
+// Per-tensor: 256x256 tiles per pair (128x256 per CTA), 6 stages of one K
+// tile; the unscale 2^-(ea+eb) is applied in the epilogue.
 // Block-scaled: the scales enter the MMA itself (kind::mxf8f6f4 with
-// block_scale, E8M0 scale per 32 K).  Tiles are 128x224 so that two
-// accumulators (448 columns) and a 16-column scale slot per pipeline stage
-// (64 columns) fit the 512 TMEM columns.  Power-of-two fp32 block scales
-// (1x128, 128x128) are re-encoded as E8M0 exactly and repeated over the four
-// 32-wide K sub-blocks they cover.  The scale writers load the scales of four
-// K tiles per 16-byte vector, one group ahead of use, and store into TMEM the
-// cells the MMA reads: the scale of A row m at lane m, column m/32; the scale
-// of B row n at lane 32q + n%32, column n/32, in every lane quarter q (each
-// quarter of the tensor core reads its own copy); byte = K sub-block.
+// block_scale, E8M0 scale per 32 K).  Tiles are 256x224 per pair so that two
+// accumulators (448 columns) and four 16-column scale slots fit the 512 TMEM
+// columns; stages hold two K tiles.  Power-of-two fp32 block scales (1x128,
+// 128x128) are re-encoded as E8M0 exactly and repeated over the four 32-wide K
+// sub-blocks they cover.  The scale writers store into TMEM the cells the MMA
+// reads: the scale of A row m at lane m, column m/32; the scale of B row n at
+// lane 32q + n%32, column n/32, in every lane quarter q (each quarter of the
+// tensor core reads its own copy); byte = K sub-block.
 //
 // Every barrier wait is bounded (2 s); a wait that gives up raises a shared
 // abort flag, every role leaves its loop, in-flight TMA loads and MMAs are
