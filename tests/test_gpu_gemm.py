@@ -125,7 +125,8 @@ def pow2_scales(rng, shape):
     return np.ldexp(np.float32(1), rng.integers(-10, 10, shape)).astype(np.float32)
 
 
-BS_SHAPES = [(128, 256, 128), (256, 512, 512), (200, 272, 384), (384, 1024, 1024), (128, 256, 2048)]
+BS_SHAPES = [(128, 256, 128), (256, 512, 512), (200, 272, 384), (384, 1024, 1024), (128, 256, 2048),
+             (520, 784, 2048)]
 
 
 @pytest.mark.parametrize("M,N,K", BS_SHAPES)
