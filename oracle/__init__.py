@@ -13,7 +13,9 @@ What each function computes, and the passage it follows, is stated in
   and activations, "FP8_E5" for gradients: "Training and inference of large
   language models using 8-bit floating point", "Proposed method"), RNE with
   saturation to the largest finite magnitude.
-* ``compute_bias`` -- floor(log2(fmax / amax)) - margin (same section).
+* ``compute_bias`` -- floor(log2(fmax / amax)) - margin (same section);
+  ``compute_bias_ocp`` and ``scale_ratio`` are the two alternatives kept
+  behind options (the OCP MX rule for 1x32 blocks, and s = fmax / amax).
 * ``quantize_tensor`` / ``quantize_block`` -- Encode(x * 2^e), per tensor or per
   block ("Per-Tensor and Per-Block Scaling Strategies for Effective FP8
   Training", "Key Questions Answered").
@@ -42,7 +44,7 @@ _SRC = os.path.join(_HERE, "fp8_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
 E4M3, E5M2 = 0, 1
-TENSOR, BLOCK_1x128, BLOCK_128x128, MX_1x32 = 0, 1, 2, 3
+TENSOR, BLOCK_1x128, BLOCK_128x128, MX_1x32, MX_1x32_OCP = 0, 1, 2, 3, 4
 FMAX = {E4M3: 448.0, E5M2: 57344.0}
 
 _lock = threading.Lock()
@@ -76,6 +78,10 @@ def lib() -> ctypes.CDLL:
             L.fp8o_decode_array.argtypes = [vp, i64, i32, vp]
             L.fp8o_compute_bias.restype = i32
             L.fp8o_compute_bias.argtypes = [f32, i32, i32, ctypes.POINTER(ctypes.c_int)]
+            L.fp8o_compute_bias_ocp.restype = i32
+            L.fp8o_compute_bias_ocp.argtypes = [f32, i32, i32, ctypes.POINTER(ctypes.c_int)]
+            L.fp8o_compute_scale_ratio.restype = i32
+            L.fp8o_compute_scale_ratio.argtypes = [f32, i32, vp, vp]
             L.fp8o_amax.restype = f32
             L.fp8o_amax.argtypes = [vp, i64, i64, i64]
             L.fp8o_quantize_tensor.argtypes = [vp, i64, i64, i64, i32, f32, vp, vp]
@@ -149,6 +155,21 @@ def pow2f(e: int) -> np.float32:
     return np.float32(np.ldexp(np.float32(1.0), int(e)))
 
 
+def compute_bias_ocp(amax: float, fmt: int, margin: int = 0) -> tuple[int, bool]:
+    """The OCP MX alternative: e = emax - floor(log2 amax) - margin (emax 8 for E4M3, 15 for E5M2)."""
+    nf = ctypes.c_int(0)
+    e = lib().fp8o_compute_bias_ocp(float(np.float32(amax)), fmt, int(margin), ctypes.byref(nf))
+    return int(e), bool(nf.value)
+
+
+def scale_ratio(amax: float, fmt: int) -> tuple[np.float32, np.float32, bool]:
+    """The non-power-of-two alternative: (s = fmax / amax, 1 / s, nonfinite), fp32 divisions."""
+    s = np.zeros(1, np.float32)
+    si = np.zeros(1, np.float32)
+    nf = lib().fp8o_compute_scale_ratio(float(np.float32(amax)), fmt, _p(s), _p(si))
+    return s[0], si[0], bool(nf)
+
+
 def scale_triple(amax: float, fmt: int, margin: int = 0) -> tuple[int, np.float32, np.float32]:
     e, _ = compute_bias(amax, fmt, margin)
     return e, pow2f(e), pow2f(-e)
@@ -175,7 +196,7 @@ def quantize_tensor(x_bf16: np.ndarray, fmt: int, scale: float, row: bool = True
 
 
 def block_shape(gran: int) -> tuple[int, int]:
-    return {BLOCK_1x128: (1, 128), BLOCK_128x128: (128, 128), MX_1x32: (1, 32)}[gran]
+    return {BLOCK_1x128: (1, 128), BLOCK_128x128: (128, 128), MX_1x32: (1, 32), MX_1x32_OCP: (1, 32)}[gran]
 
 
 def scale_shapes(rows: int, cols: int, gran: int) -> tuple[tuple[int, int], tuple[int, int]]:
@@ -191,7 +212,7 @@ def quantize_block(x_bf16: np.ndarray, fmt: int, gran: int, margin: int = 0, row
     x = np.ascontiguousarray(x_bf16).view(np.uint16)
     r, c = x.shape
     srow, scol = scale_shapes(r, c, gran)
-    sdt = np.uint8 if gran == MX_1x32 else np.float32
+    sdt = np.uint8 if gran in (MX_1x32, MX_1x32_OCP) else np.float32
     qr = np.empty((r, c), np.uint8) if row else None
     sr = np.empty(srow, sdt) if row else None
     qc = np.empty((c, r), np.uint8) if col else None
@@ -227,7 +248,7 @@ class HistoryState:
 def _sf_arg(gran: int, sf) -> np.ndarray:
     if gran == TENSOR:
         return np.array([sf], np.float32).reshape(1) if np.isscalar(sf) else np.ascontiguousarray(sf, np.float32)
-    if gran == MX_1x32:
+    if gran in (MX_1x32, MX_1x32_OCP):
         return np.ascontiguousarray(sf, np.uint8)
     return np.ascontiguousarray(sf, np.float32)
 

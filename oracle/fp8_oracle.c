@@ -52,6 +52,7 @@
 #define GRAN_1x128 1
 #define GRAN_128x128 2
 #define GRAN_MX32 3
+#define GRAN_MX32_OCP 4 /* 1x32 blocks, E8M0, the OCP MX bias rule */
 
 /* ------------------------------------------------------------------ formats */
 
@@ -171,6 +172,41 @@ int fp8o_compute_bias(float amax, int fmt, int margin, int *nonfinite)
 
 float fp8o_pow2f(int e) { return ldexpf(1.0f, e); }
 
+/* The OCP MX alternative to compute_bias for MX blocks, not the default: the
+ * block's largest magnitude is moved into the top binade of the format,
+ * e = emax - floor(log2(amax)) - margin with emax = 8 (E4M3) or 15 (E5M2), so a
+ * block whose amax has a significand above 1.75 saturates.  Same clamping and
+ * special cases as compute_bias.  floor(log2(amax)) is read off frexp. */
+int fp8o_compute_bias_ocp(float amax, int fmt, int margin, int *nonfinite)
+{
+    if (isnan(amax) || isinf(amax)) {
+        if (nonfinite) *nonfinite = 1;
+        return 0;
+    }
+    double a = fabs((double)amax);
+    if (a == 0.0) return 0;
+    int x;
+    frexp(a, &x);
+    long e = (long)(fmt == FMT_E4M3 ? 8 : 15) - (long)(x - 1) - (long)margin;
+    if (e < -126) e = -126;
+    if (e > 127) e = 127;
+    return (int)e;
+}
+
+/* The non-power-of-two alternative for per-tensor scales, not the default:
+ * s = fmax / amax and s_inv = 1 / s, each one fp32 division rounded to nearest
+ * (so the cast rounds twice: the product x s, then Encode).  amax == 0 gives
+ * s = 1; a non-finite amax gives s = 1 and returns 1. */
+int fp8o_compute_scale_ratio(float amax, int fmt, float *scale, float *scale_inv)
+{
+    int nf = isnan(amax) || isinf(amax);
+    float a = fabsf(amax);
+    float s = (nf || a == 0.0f) ? 1.0f : (float)fmt_max(fmt) / a;
+    *scale = s;
+    *scale_inv = 1.0f / s;
+    return nf;
+}
+
 /* ------------------------------------------------------------------ amax */
 
 /* max |x| over a bf16 matrix; a NaN anywhere makes the result NaN */
@@ -214,7 +250,7 @@ void fp8o_quantize_tensor(const uint16_t *x, int64_t rows, int64_t cols, int64_t
  * The stored scale is the dequantisation factor 2^-e_b, as fp32 (sf_f32) or as
  * the E8M0 code 127 - e_b (sf_e8m0), at [block_row * nbc + block_col]. */
 static void quant_blocks(const uint16_t *x, int64_t rows, int64_t cols, int64_t rs, int64_t cs, int fmt,
-                         int margin, int64_t br, int64_t bc, uint8_t *q, float *sf_f32, uint8_t *sf_e8m0,
+                         int margin, int64_t br, int64_t bc, int ocp, uint8_t *q, float *sf_f32, uint8_t *sf_e8m0,
                          int *nonfinite)
 {
     int64_t nbr = (rows + br - 1) / br, nbc = (cols + bc - 1) / bc;
@@ -227,7 +263,7 @@ static void quant_blocks(const uint16_t *x, int64_t rows, int64_t cols, int64_t 
         int64_t nj = cols - j0 < bc ? cols - j0 : bc;
         float amax = amax_of(x + i0 * rs + j0 * cs, ni, nj, rs, cs);
         int nf = 0;
-        int e = fp8o_compute_bias(amax, fmt, margin, &nf);
+        int e = ocp ? fp8o_compute_bias_ocp(amax, fmt, margin, &nf) : fp8o_compute_bias(amax, fmt, margin, &nf);
         flag |= nf;
         float s = ldexpf(1.0f, e);
         for (int64_t i = i0; i < i0 + ni; ++i)
@@ -246,26 +282,28 @@ static void gran_block(int gran, int64_t *br, int64_t *bc)
     switch (gran) {
     case GRAN_1x128: *br = 1; *bc = 128; break;
     case GRAN_128x128: *br = 128; *bc = 128; break;
-    default: *br = 1; *bc = 32; break; /* MX 1x32 */
+    default: *br = 1; *bc = 32; break; /* MX 1x32, either bias rule */
     }
 }
 
 /* Block granularities.  Row-wise output: blocks over x as stored.
  * Column-wise output: the same quantisation applied to x transposed, so
  * 1x128 -> 128x1 blocks down the columns, 1x32 -> 32x1, 128x128 unchanged.
- * Scales are fp32 2^-e (1x128, 128x128) or E8M0 codes (1x32). */
+ * Scales are fp32 2^-e (1x128, 128x128) or E8M0 codes (1x32; granularity 4 is
+ * 1x32 with the OCP MX bias rule). */
 int fp8o_quantize_block(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld, int fmt, int gran, int margin,
                         uint8_t *q_row, void *sf_row, uint8_t *q_col, void *sf_col)
 {
     int64_t br, bc;
     gran_block(gran, &br, &bc);
-    int mx = gran == GRAN_MX32;
+    int mx = gran == GRAN_MX32 || gran == GRAN_MX32_OCP;
+    int ocp = gran == GRAN_MX32_OCP;
     int nf = 0;
     if (q_row)
-        quant_blocks(x, rows, cols, ld, 1, fmt, margin, br, bc, q_row, mx ? NULL : (float *)sf_row,
+        quant_blocks(x, rows, cols, ld, 1, fmt, margin, br, bc, ocp, q_row, mx ? NULL : (float *)sf_row,
                      mx ? (uint8_t *)sf_row : NULL, &nf);
     if (q_col)
-        quant_blocks(x, cols, rows, 1, ld, fmt, margin, br, bc, q_col, mx ? NULL : (float *)sf_col,
+        quant_blocks(x, cols, rows, 1, ld, fmt, margin, br, bc, ocp, q_col, mx ? NULL : (float *)sf_col,
                      mx ? (uint8_t *)sf_col : NULL, &nf);
     return nf;
 }
