@@ -71,7 +71,8 @@ typedef enum {
     FP8_SCALE_TENSOR = 0,        /* one scale for the whole tensor */
     FP8_SCALE_BLOCK_1x128 = 1,   /* activation blocks: 1 row x 128 columns */
     FP8_SCALE_BLOCK_128x128 = 2, /* weight blocks: 128 x 128 */
-    FP8_SCALE_MX_1x32 = 3        /* MXFP8: 1 x 32 blocks, E8M0 scales */
+    FP8_SCALE_MX_1x32 = 3,       /* MXFP8: 1 x 32 blocks, E8M0 scales */
+    FP8_SCALE_MX_1x32_OCP = 4    /* the same blocks and storage with the OCP MX bias rule (option) */
 } fp8_granularity;
 
 typedef enum { FP8_GEMM_FPROP = 0, FP8_GEMM_DGRAD = 1, FP8_GEMM_WGRAD = 2 } fp8_gemm_op;
@@ -116,6 +117,26 @@ FP8Q_API fp8_status fp8_amax(const void *x, int64_t rows, int64_t cols, int64_t 
  */
 FP8Q_API fp8_status fp8_compute_scale(const float *amax, fp8_format fmt, int32_t margin, int32_t *bias, float *scale,
                              float *scale_inv, int32_t *status, void *stream);
+
+/*
+ * fp8_compute_scale_ratio -- the non-power-of-two alternative to compute_bias.
+ * Source: the scale taken as the ratio of the format maximum to the tensor's
+ * amax itself, the quantity whose logarithm the compute_bias rule floors
+ * ("Training and inference of large language models using 8-bit floating
+ * point", "Proposed method").  Not the default.
+ *
+ *   scale = fmax / amax, scale_inv = 1 / scale, each one fp32 division rounded
+ *   to nearest; amax == 0 gives 1, 1; a non-finite amax gives 1, 1 and sets
+ *   FP8_STATUS_NONFINITE_AMAX.  A cast with such a scale rounds twice (the
+ *   fp32 product, then the FP8 encoding); fp8_quantize and fp8_scaled_gemm take
+ *   it like any per-tensor scale.
+ *
+ *   amax       device, one fp32 (read).
+ *   scale, scale_inv: device, one fp32 each (written; either may be NULL, not both).
+ *   status     device int32 or NULL.
+ */
+FP8Q_API fp8_status fp8_compute_scale_ratio(const float *amax, fp8_format fmt, float *scale, float *scale_inv,
+                                            int32_t *status, void *stream);
 
 /*
  * fp8_amax_history_update -- one delayed-scaling step.
@@ -193,6 +214,11 @@ FP8Q_API fp8_status fp8_cast_stats(const void *x, int64_t rows, int64_t cols, in
  *              sf_row and sf_col must be NULL.
  *            FP8_SCALE_BLOCK_1x128 / _128x128 / FP8_SCALE_MX_1x32: each block
  *              gets e_b = compute_bias(amax_b, fmt, margin); `scale` must be NULL.
+ *            FP8_SCALE_MX_1x32_OCP: MX blocks with the alternative rule of the
+ *              OCP MX format, e_b = emax - floor(log2(amax_b)) - margin (emax 8
+ *              for E4M3, 15 for E5M2): the block's largest magnitude lands in
+ *              the format's top binade and saturates when its significand
+ *              exceeds 1.75.  Not the default; scales stored as for MX.
  *              A partial block at an edge uses the elements that exist.
  *   margin   used by the block granularities only.
  *   q_row    device u8 [rows x cols] (dense), or NULL.
@@ -205,7 +231,7 @@ FP8Q_API fp8_status fp8_cast_stats(const void *x, int64_t rows, int64_t cols, in
  *   sf_row   block scales of q_row (required iff q_row and gran != TENSOR):
  *              1x128:   fp32 [rows x ceil(cols/128)]
  *              128x128: fp32 [ceil(rows/128) x ceil(cols/128)]
- *              MX 1x32: u8 E8M0 [rows x ceil(cols/32)]
+ *              MX 1x32 (either rule): u8 E8M0 [rows x ceil(cols/32)]
  *   sf_col   block scales of q_col (required iff q_col and gran != TENSOR):
  *              1x128:   fp32 [cols x ceil(rows/128)]
  *              128x128: fp32 [ceil(cols/128) x ceil(rows/128)]

@@ -26,15 +26,15 @@ LIB_PATH = os.path.join(_PKG, "libfp8q.so")
 # enums of include/fp8q.h
 FP8_OK, FP8_ERR_INVALID_ARG, FP8_ERR_UNSUPPORTED, FP8_ERR_CUDA, FP8_ERR_TIMEOUT = 0, 1, 2, 3, 4
 E4M3, E5M2 = 0, 1
-TENSOR, BLOCK_1x128, BLOCK_128x128, MX_1x32 = 0, 1, 2, 3
+TENSOR, BLOCK_1x128, BLOCK_128x128, MX_1x32, MX_1x32_OCP = 0, 1, 2, 3, 4
 FPROP, DGRAD, WGRAD = 0, 1, 2
 OUT_F32, OUT_BF16 = 0, 1
 STATUS_NONFINITE_AMAX, STATUS_TIMEOUT, STATUS_BAD_BLOCK_SCALE = 1, 2, 4
 
 # every entry point declared in include/fp8q.h
-ENTRY_POINTS = ("fp8_amax", "fp8_compute_scale", "fp8_amax_history_update", "fp8_set_bias", "fp8_cast_stats",
-                "fp8_quantize", "fp8_quantize_current",
-                "fp8_quantize_current_noalloc", "fp8_scaled_gemm", "fp8_scaled_gemm_quantize", "fp8_status_string", "fp8_last_error_detail")
+ENTRY_POINTS = ("fp8_amax", "fp8_compute_scale", "fp8_compute_scale_ratio", "fp8_amax_history_update",
+                "fp8_set_bias", "fp8_cast_stats", "fp8_quantize", "fp8_quantize_current", "fp8_quantize_current_noalloc",
+                "fp8_scaled_gemm", "fp8_scaled_gemm_quantize", "fp8_status_string", "fp8_last_error_detail")
 QUANTIZE_CURRENT_WORKSPACE_BYTES = 4096  # FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES
 
 
@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             for name, args in {
                 "fp8_amax": [vp, i64, i64, i64, vp, vp],
                 "fp8_compute_scale": [vp, i32, i32, vp, vp, vp, vp, vp],
+                "fp8_compute_scale_ratio": [vp, i32, vp, vp, vp, vp],
                 "fp8_amax_history_update": [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp],
                 "fp8_quantize": [vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp],
                 "fp8_set_bias": [i32, vp, vp, vp, vp],
@@ -129,6 +130,13 @@ def fp8_compute_scale(amax: Ptr, fmt: int, margin: int, bias: Ptr = None, scale:
                       scale_inv: Ptr = None, status: Ptr = None, stream=None) -> None:
     _check("fp8_compute_scale", lib().fp8_compute_scale(_p(amax), fmt, margin, _p(bias), _p(scale), _p(scale_inv),
                                                         _p(status), _stream(stream)))
+
+
+def fp8_compute_scale_ratio(amax: Ptr, fmt: int, scale: Ptr = None, scale_inv: Ptr = None, status: Ptr = None,
+                            stream=None) -> None:
+    """The non-power-of-two alternative: scale = fmax / amax, scale_inv = 1 / scale (fp32, nearest)."""
+    _check("fp8_compute_scale_ratio", lib().fp8_compute_scale_ratio(_p(amax), fmt, _p(scale), _p(scale_inv),
+                                                                    _p(status), _stream(stream)))
 
 
 def fp8_amax_history_update(history: torch.Tensor, pos: Ptr, amax: Ptr, fmt: int, margin: int, bias: Ptr,
@@ -214,9 +222,10 @@ def fp8_scaled_gemm_quantize(op: int, A: torch.Tensor, fa: int, sfa: Ptr, B: tor
                                           fd, _p(scale_d), _p(amax_d), _p(status), _stream(stream)))
 
 
-__all__ = ["lib", "FP8Error", "status_name", "fp8_amax", "fp8_compute_scale", "fp8_amax_history_update",
+__all__ = ["lib", "FP8Error", "status_name", "fp8_amax", "fp8_compute_scale", "fp8_compute_scale_ratio",
+           "fp8_amax_history_update",
            "fp8_set_bias", "fp8_cast_stats",
            "fp8_quantize", "fp8_quantize_current", "fp8_quantize_current_noalloc",
            "current_workspace", "fp8_scaled_gemm", "fp8_scaled_gemm_quantize", "ENTRY_POINTS",
            "QUANTIZE_CURRENT_WORKSPACE_BYTES", "LIB_PATH", "E4M3", "E5M2", "TENSOR", "BLOCK_1x128",
-           "BLOCK_128x128", "MX_1x32", "FPROP", "DGRAD", "WGRAD", "OUT_F32", "OUT_BF16"]
+           "BLOCK_128x128", "MX_1x32", "MX_1x32_OCP", "FPROP", "DGRAD", "WGRAD", "OUT_F32", "OUT_BF16"]

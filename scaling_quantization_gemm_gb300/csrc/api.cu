@@ -21,6 +21,8 @@ void set_error_detail(const char* fmt, ...) {
 fp8_status launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* amax, cudaStream_t st);
 fp8_status launch_compute_scale(const float* amax, int fmt, int margin, int32_t* bias, float* scale, float* scale_inv,
                                 int32_t* status, cudaStream_t st);
+fp8_status launch_compute_scale_ratio(const float* amax, int fmt, float* scale, float* scale_inv, int32_t* status,
+                                      cudaStream_t st);
 fp8_status launch_history(float* hist, int len, int64_t* pos, float* amax, int fmt, int margin, int32_t* bias,
                           float* scale, float* scale_inv, int32_t* status, cudaStream_t st);
 fp8_status launch_quantize_current(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int margin,
@@ -43,7 +45,7 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool valid_fmt(int f) { return f == FP8_E4M3 || f == FP8_E5M2; }
-bool valid_gran(int g) { return g >= FP8_SCALE_TENSOR && g <= FP8_SCALE_MX_1x32; }
+bool valid_gran(int g) { return g >= FP8_SCALE_TENSOR && g <= FP8_SCALE_MX_1x32_OCP; }
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 fp8_status check_bf16_matrix(const void* x, int64_t rows, int64_t cols, int64_t ld) {
@@ -96,6 +98,15 @@ fp8_status fp8_compute_scale(const float* amax, fp8_format fmt, int32_t margin, 
     return launch_compute_scale(amax, fmt, margin, bias, scale, scale_inv, status, as_stream(stream));
 }
 
+fp8_status fp8_compute_scale_ratio(const float* amax, fp8_format fmt, float* scale, float* scale_inv, int32_t* status,
+                                   void* stream) {
+    g_detail[0] = 0;
+    FP8_REQUIRE(amax != nullptr, FP8_ERR_INVALID_ARG, "amax is NULL");
+    FP8_REQUIRE(valid_fmt(fmt), FP8_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
+    FP8_REQUIRE(scale || scale_inv, FP8_ERR_INVALID_ARG, "no output (scale and scale_inv both NULL)");
+    return launch_compute_scale_ratio(amax, fmt, scale, scale_inv, status, as_stream(stream));
+}
+
 fp8_status fp8_amax_history_update(float* history, int32_t len, int64_t* pos, float* amax, fp8_format fmt,
                                    int32_t margin, int32_t* bias, float* scale, float* scale_inv, int32_t* status,
                                    void* stream) {
@@ -127,7 +138,7 @@ fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, f
         FP8_REQUIRE(!q_col || sf_col, FP8_ERR_INVALID_ARG, "q_col needs sf_col");
         FP8_REQUIRE(!sf_row || q_row, FP8_ERR_INVALID_ARG, "sf_row given without q_row");
         FP8_REQUIRE(!sf_col || q_col, FP8_ERR_INVALID_ARG, "sf_col given without q_col");
-        const uintptr_t sa = gran == FP8_SCALE_MX_1x32 ? 1 : 4;
+        const uintptr_t sa = (gran == FP8_SCALE_MX_1x32 || gran == FP8_SCALE_MX_1x32_OCP) ? 1 : 4;
         FP8_REQUIRE((!sf_row || aligned(sf_row, sa)) && (!sf_col || aligned(sf_col, sa)), FP8_ERR_INVALID_ARG,
                     "block scale tensors must be aligned to their element size");
     }

@@ -80,6 +80,30 @@ __host__ __device__ __forceinline__ int bias_from_amax(float amax, int fmt, int 
 }
 
 // 2^e as an exact fp32 for e in [-149, 127].
+// The OCP MX alternative, e = emax - floor(log2(amax)) - margin (emax = 8 for
+// E4M3, 15 for E5M2), from the exponent bits; same special cases and clamping.
+__host__ __device__ __forceinline__ int bias_from_amax_ocp(float amax, int fmt, int margin, bool* nonfinite) {
+    uint32_t u;
+#ifdef __CUDA_ARCH__
+    u = __float_as_uint(amax) & 0x7FFFFFFFu;
+#else
+    __builtin_memcpy(&u, &amax, 4);
+    u &= 0x7FFFFFFFu;
+#endif
+    if (u >= 0x7F800000u) {
+        *nonfinite = true;
+        return 0;
+    }
+    if (u == 0) return 0;
+    int ea = (int)(u >> 23) - 127;
+    if ((u >> 23) == 0) {  // subnormal: floor(log2) from the leading mantissa bit
+        ea = -127;
+        for (uint32_t m = u; m < 0x00400000u; m <<= 1) --ea;
+    }
+    int e = (fmt == FP8_E4M3 ? 8 : 15) - ea - margin;
+    return e < -126 ? -126 : (e > 127 ? 127 : e);
+}
+
 __host__ __device__ __forceinline__ float pow2_exact(int e) {
     uint32_t u = (e >= -126) ? ((uint32_t)(e + 127) << 23) : (1u << (e + 149));
 #ifdef __CUDA_ARCH__

@@ -1190,7 +1190,8 @@ fp8_status launch_single(const CUtensorMap& tmA, const CUtensorMap& tmB, const G
     return check_launch("gemm_tensor_kernel launch");
 }
 
-int sf_kind(int gran) { return gran == FP8_SCALE_MX_1x32 ? SF_MX : gran == FP8_SCALE_BLOCK_1x128 ? SF_ROW : SF_BLOCK; }
+bool is_mx(int gran) { return gran == FP8_SCALE_MX_1x32 || gran == FP8_SCALE_MX_1x32_OCP; }  // same E8M0 storage
+int sf_kind(int gran) { return is_mx(gran) ? SF_MX : gran == FP8_SCALE_BLOCK_1x128 ? SF_ROW : SF_BLOCK; }
 
 template <int OUT_BF16, int KA, int KB>
 fp8_status launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g, uint32_t idesc, int grid,
@@ -1299,10 +1300,10 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
     g.sfb = sfb;
     const int64_t KT = (K + BK - 1) / BK;
     // row pitch of each scale tensor: E8M0 rows are K/32 bytes, fp32 rows are ceil(K/128) floats
-    g.sfa_ld = (ga == FP8_SCALE_MX_1x32) ? K / 32 : KT;
-    g.sfb_ld = (gb == FP8_SCALE_MX_1x32) ? K / 32 : KT;
+    g.sfa_ld = is_mx(ga) ? K / 32 : KT;
+    g.sfb_ld = is_mx(gb) ? K / 32 : KT;
     auto vec_ok = [](const void* p, int gran, int64_t ld) {
-        const int64_t row_bytes = gran == FP8_SCALE_MX_1x32 ? ld : 4 * ld;
+        const int64_t row_bytes = is_mx(gran) ? ld : 4 * ld;
         return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && row_bytes % 16 == 0;
     };
     g.vec_a = vec_ok(sfa, ga, g.sfa_ld);

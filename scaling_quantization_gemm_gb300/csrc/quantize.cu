@@ -72,6 +72,26 @@ __device__ __forceinline__ int bias_bf16(uint32_t m, int fmt, int margin) {
     return bias_from_amax(bf16bits_to_float(m), fmt, margin, &nf);
 }
 
+// The OCP MX alternative for 1x32 blocks: e = emax - floor(log2(amax)) - margin, no mantissa term.
+__device__ __forceinline__ int bias_bf16_ocp(uint32_t m, int fmt, int margin) {
+    if (m - 0x80u < 0x7F00u) {
+        const int ef = fmt == FP8_E4M3 ? 8 : 15;
+        const int e = ef + 127 - (int)(m >> 7) - margin;
+        return min(max(e, -126), 127);
+    }
+    bool nf = false;
+    return bias_from_amax_ocp(bf16bits_to_float(m), fmt, margin, &nf);
+}
+
+// Block bias of granularity GRAN.
+template <int GRAN>
+__device__ __forceinline__ int block_bias(uint32_t m, int fmt, int margin) {
+    if constexpr (GRAN == FP8_SCALE_MX_1x32_OCP)
+        return bias_bf16_ocp(m, fmt, margin);
+    else
+        return bias_bf16(m, fmt, margin);
+}
+
 // Running |x| maximum of bf16 pairs: one instruction per word.  max.xorsign.abs
 // keeps the larger magnitude (its sign bit is meaningless and masked off at the
 // end); .NaN makes a NaN win, so a NaN input yields a NaN amax.
@@ -180,7 +200,8 @@ __device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const Qua
 
     // tiles that need a block-wide reduction keep the CTA in lock step (MX column scales: the four
     // 32-row segments of a column come from four warps and leave as one 4-byte store)
-    const bool lockstep = GRAN == FP8_SCALE_BLOCK_128x128 || ((GRAN == FP8_SCALE_BLOCK_1x128 || GRAN == FP8_SCALE_MX_1x32) && a.do_col);
+    constexpr bool kMX = GRAN == FP8_SCALE_MX_1x32 || GRAN == FP8_SCALE_MX_1x32_OCP;
+    const bool lockstep = GRAN == FP8_SCALE_BLOCK_128x128 || ((GRAN == FP8_SCALE_BLOCK_1x128 || kMX) && a.do_col);
     if (tid == 0) {
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(smem_u32(&S.full[s]), 1);
@@ -279,11 +300,11 @@ __device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const Qua
                     s2 = s2_tensor;
                 } else if constexpr (GRAN == FP8_SCALE_BLOCK_128x128) {
                     s2 = pow2_bf16x2(e_tile);
-                } else if constexpr (GRAN == FP8_SCALE_MX_1x32) {
+                } else if constexpr (kMX) {
                     uint32_t m = cm[k];
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                    const int e = bias_bf16(m, FMT, a.margin);
+                    const int e = block_bias<GRAN>(m, FMT, a.margin);
                     s2 = pow2_bf16x2(e);
                     if ((j & 3) == 0 && okr)
                         static_cast<uint8_t*>(a.sf_row)[r * cdiv(a.cols, 32) + (col >> 5)] = (uint8_t)(127 - e);
@@ -328,9 +349,9 @@ __device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const Qua
                 sA = sB = s2_tensor;
             } else if constexpr (GRAN == FP8_SCALE_BLOCK_128x128) {
                 sA = sB = pow2_bf16x2(e_tile);
-            } else if constexpr (GRAN == FP8_SCALE_MX_1x32) {
-                const int eA = bias_bf16(mm & 0xFFFFu, FMT, a.margin);
-                const int eB = bias_bf16(mm >> 16, FMT, a.margin);
+            } else if constexpr (kMX) {
+                const int eA = block_bias<GRAN>(mm & 0xFFFFu, FMT, a.margin);
+                const int eB = block_bias<GRAN>(mm >> 16, FMT, a.margin);
                 sA = pow2_bf16x2(eA);
                 sB = pow2_bf16x2(eB);
                 uint8_t* cs = reinterpret_cast<uint8_t*>(S.col_sf[parity]);
@@ -568,6 +589,17 @@ __global__ void compute_scale_kernel(const float* amax, int fmt, int margin, int
     if (nf && status) atomicOr(status, FP8_STATUS_NONFINITE_AMAX);
 }
 
+// The ratio alternative: scale = fmax / amax, scale_inv = 1 / scale, each rounded to nearest.
+__global__ void compute_scale_ratio_kernel(const float* amax, int fmt, float* scale, float* scale_inv,
+                                           int32_t* status) {
+    const float a = fabsf(*amax);
+    const bool nf = !(a <= 3.402823466e38f);  // NaN or Inf
+    const float s = (nf || a == 0.0f) ? 1.0f : __fdiv_rn(fmt == FP8_E4M3 ? 448.0f : 57344.0f, a);
+    if (scale) *scale = s;
+    if (scale_inv) *scale_inv = __fdiv_rn(1.0f, s);
+    if (nf && status) atomicOr(status, FP8_STATUS_NONFINITE_AMAX);
+}
+
 // One delayed-scaling step in one CTA: record, window max, bias, reset.
 __global__ void __launch_bounds__(1024) history_kernel(float* hist, int len, int64_t* pos, float* amax, int fmt,
                                                        int margin, int32_t* bias, float* scale, float* scale_inv,
@@ -671,6 +703,12 @@ fp8_status launch_compute_scale(const float* amax, int fmt, int margin, int32_t*
                                 float* scale_inv, int32_t* status, cudaStream_t st) {
     compute_scale_kernel<<<1, 1, 0, st>>>(amax, fmt, margin, bias, scale, scale_inv, status);
     return check_launch("compute_scale kernel launch");
+}
+
+fp8_status launch_compute_scale_ratio(const float* amax, int fmt, float* scale, float* scale_inv, int32_t* status,
+                                      cudaStream_t st) {
+    compute_scale_ratio_kernel<<<1, 1, 0, st>>>(amax, fmt, scale, scale_inv, status);
+    return check_launch("compute_scale_ratio kernel launch");
 }
 
 fp8_status launch_history(float* hist, int len, int64_t* pos, float* amax, int fmt, int margin, int32_t* bias,
@@ -785,6 +823,7 @@ fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld
         FP8Q_QDISPATCH(FP8_SCALE_BLOCK_1x128)
         FP8Q_QDISPATCH(FP8_SCALE_BLOCK_128x128)
         FP8Q_QDISPATCH(FP8_SCALE_MX_1x32)
+        FP8Q_QDISPATCH(FP8_SCALE_MX_1x32_OCP)
     }
 #undef FP8Q_QDISPATCH
     return FP8_ERR_UNSUPPORTED;

@@ -36,9 +36,10 @@ from typing import Optional
 
 import torch
 
-from . import (BLOCK_1x128, BLOCK_128x128, DGRAD, E4M3, E5M2, FPROP, MX_1x32, TENSOR, WGRAD, current_workspace,
-               fp8_amax, fp8_amax_history_update, fp8_cast_stats, fp8_compute_scale, fp8_quantize,
-               fp8_quantize_current, fp8_scaled_gemm, fp8_scaled_gemm_quantize, fp8_set_bias)
+from . import (BLOCK_1x128, BLOCK_128x128, DGRAD, E4M3, E5M2, FPROP, MX_1x32, MX_1x32_OCP, TENSOR, WGRAD,
+               current_workspace, fp8_amax, fp8_amax_history_update, fp8_cast_stats, fp8_compute_scale,
+               fp8_compute_scale_ratio, fp8_quantize, fp8_quantize_current, fp8_scaled_gemm, fp8_scaled_gemm_quantize,
+               fp8_set_bias)
 
 
 class ScaleState:
@@ -100,10 +101,13 @@ def gemm_flops(m: int, n: int, k: int) -> float:
 
 @dataclass
 class PerTensorFwd:
-    """Per-tensor current-scaling forward: Y[M x N] fp32 = unscale(Q(X) Q(W)^T)."""
+    """Per-tensor current-scaling forward: Y[M x N] fp32 = unscale(Q(X) Q(W)^T).  `scale_rule`
+    "pow2" is the compute_bias rule (one fused launch per cast); "ratio" is the alternative
+    s = fmax / amax (amax, ratio, cast: three launches)."""
     X: torch.Tensor
     W: torch.Tensor
     margin: int = 0
+    scale_rule: str = "pow2"
 
     def __post_init__(self):
         dev = self.X.device
@@ -117,8 +121,14 @@ class PerTensorFwd:
         self.flops = gemm_flops(M, N, K)
 
     def run(self) -> None:
-        quantize_current(self.X, self.sx, self.ws, q_row=self.qx)
-        quantize_current(self.W, self.sw, self.ws, q_row=self.qw)
+        for x, st, q in ((self.X, self.sx, self.qx), (self.W, self.sw, self.qw)):
+            if self.scale_rule == "ratio":
+                st.amax.zero_()
+                fp8_amax(x, st.amax)
+                fp8_compute_scale_ratio(st.amax, st.fmt, st.scale, st.scale_inv, st.status)
+                fp8_quantize(x, st.fmt, TENSOR, scale=st.scale, q_row=q)
+            else:
+                quantize_current(x, st, self.ws, q_row=q)
         fp8_scaled_gemm(FPROP, self.qx, E4M3, TENSOR, self.sx.scale_inv, self.qw, E4M3, TENSOR, self.sw.scale_inv,
                         self.Y)
 
@@ -133,7 +143,11 @@ class LinearFwdBwd:
     """
 
     def __init__(self, X: torch.Tensor, W: torch.Tensor, dY: torch.Tensor, history_len: int, margin: int = 0,
-                 grad_margin: int = 0, dw_dtype=torch.float32):
+                 grad_margin: int = 0, dw_dtype=torch.float32, first_step: str = "current"):
+        # first_step: the empty-history step scales from its own amax ("current"), or with the fixed
+        # bias e = 0, scale 1 ("fixed", the alternative)
+        assert first_step in ("current", "fixed")
+        self.first_step = first_step
         dev = X.device
         M, K = X.shape
         N = W.shape[0]
@@ -156,9 +170,9 @@ class LinearFwdBwd:
     def quantize_one(self, i: int) -> None:
         x, st, qr, qc = ((self.X, self.sx, self.qx_row, self.qx_col), (self.W, self.sw, self.qw_row, self.qw_col),
                          (self.dY, self.sg, self.qg_row, self.qg_col))[i]
-        if st.steps == 0:
+        if st.steps == 0 and self.first_step == "current":
             quantize_current(x, st, self.ws, q_row=qr, q_col=qc)  # empty history: scale from its own amax
-        else:
+        else:  # delayed scale (or the initial scale 1 for a fixed first step), amax recorded
             fp8_quantize(x, st.fmt, TENSOR, scale=st.scale, q_row=qr, q_col=qc, amax=st.amax)
 
     def quantize(self) -> None:
@@ -189,13 +203,16 @@ class BlockLinearFwd:
     Y [M x N] bf16 = sum_k (QX sx)(QW sw).  With `col=True` the column-wise (transposed) copies and
     their scales are produced too, as the backward pass would need them."""
 
-    def __init__(self, X: torch.Tensor, W: torch.Tensor, mx: bool, col: bool = False, margin: int = 0):
+    def __init__(self, X: torch.Tensor, W: torch.Tensor, mx: bool, col: bool = False, margin: int = 0,
+                 mx_rule: str = "compute_bias"):
+        # mx_rule "ocp": MX blocks with the OCP MX bias rule (the alternative), same E8M0 storage
         dev = X.device
         M, K = X.shape
         N = W.shape[0]
         self.X, self.W, self.mx, self.col, self.margin = X, W, mx, col, margin
-        self.gx = MX_1x32 if mx else BLOCK_1x128
-        self.gw = MX_1x32 if mx else BLOCK_128x128
+        mxg = MX_1x32_OCP if mx_rule == "ocp" else MX_1x32
+        self.gx = mxg if mx else BLOCK_1x128
+        self.gw = mxg if mx else BLOCK_128x128
         u8 = dict(dtype=torch.uint8, device=dev)
         sdt = dict(dtype=torch.uint8 if mx else torch.float32, device=dev)
         cd = lambda a, b: (a + b - 1) // b
@@ -293,7 +310,7 @@ class PTQStack:
 
 def _scale_bytes(rows: int, cols: int, gran: int) -> int:
     cd = lambda a, b: (a + b - 1) // b
-    if gran == MX_1x32:
+    if gran in (MX_1x32, MX_1x32_OCP):
         return rows * cd(cols, 32)
     if gran == BLOCK_1x128:
         return 4 * rows * cd(cols, 128)

@@ -178,3 +178,11 @@ def test_set_bias_and_cast_stats_validation(L):
     assert cs(FAKE, 32, 32, 32, 0, FAKE, 1, FAKE + 4, FAKE, None) == 1  # counters 8-byte aligned
     assert cs(FAKE, 32, 12, 12, 0, FAKE, 1, FAKE, FAKE, None) == 2  # cols % 8
     assert cs(FAKE, 0, 32, 32, 0, FAKE, 1, FAKE, FAKE, None) == 0  # empty
+
+
+def test_compute_scale_ratio_validation(L):
+    assert L.fp8_compute_scale_ratio(None, 0, FAKE, FAKE, None, None) == 1
+    assert L.fp8_compute_scale_ratio(FAKE, 3, FAKE, FAKE, None, None) == 1
+    assert L.fp8_compute_scale_ratio(FAKE, 0, None, None, None, None) == 1
+    q = L.fp8_quantize
+    assert q(FAKE, 32, 32, 32, 0, 5, 0, None, FAKE, None, FAKE, None, None, None) == 1  # granularity 5 unknown
