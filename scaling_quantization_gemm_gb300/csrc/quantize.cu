@@ -12,7 +12,10 @@
 // a two-deep TMA ring per CTA, three CTAs per SM (up to six tile loads in
 // flight per SM), computes block maxima in registers (warp shuffles), writes
 // the row-wise codes, and reads the same tile down its columns for the
-// transposed column-wise codes, so one HBM read feeds both outputs.  The fused
+// transposed column-wise codes, so one HBM read feeds both outputs.  The
+// column-wise codes of a tile are staged (128B-swizzled) in the tile's own
+// shared-memory stage once every warp has read it, and leave as one TMA store
+// of whole 128-byte lines; the stage is refilled after that store has read it.  The fused
 // amax is reduced per warp, per CTA, then one atomic per CTA.  Current scaling
 // runs the amax pass and the cast in one cooperative launch with a grid
 // barrier between them.
@@ -20,6 +23,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -44,6 +48,13 @@ struct QuantArgs {
     int64_t tiles_c, ntiles;
     int do_row, do_col;
     int32_t* status;
+};
+
+// Tensor maps of a cast launch: the bf16 input x and the column-wise output (u8 [cols x rows]; unused
+// without one).
+struct QuantMaps {
+    CUtensorMap x;
+    CUtensorMap qc;
 };
 
 struct alignas(1024) QuantSmem {
@@ -174,23 +185,28 @@ __device__ __forceinline__ void encode_column32_f32(const uint32_t (&w)[32], flo
     }
 }
 
-__device__ __forceinline__ void store_col32(uint8_t* q_col, int64_t c, int64_t rows, int64_t row0,
-                                            const uint32_t (&o)[8]) {
-    uint8_t* dst = q_col + c * rows + row0;
-    if (row0 < rows) *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
-    if (row0 + 16 < rows) *reinterpret_cast<uint4*>(dst + 16) = make_uint4(o[4], o[5], o[6], o[7]);
+// The 32 codes of column c (0..127 in the tile), rows 32 seg .. 32 seg + 31, into the staged
+// column-wise tile: 128 bytes per column, 16-byte chunks in the 128B swizzle of the TMA store
+// (chunk k of line c sits at chunk k ^ (c % 8); the stage is 1024-byte aligned).
+__device__ __forceinline__ void stage_col32(uint32_t base, int c, int seg, const uint32_t (&o)[8]) {
+    const uint32_t line = base + (uint32_t)c * kTile;
+    st_shared_v4(line + ((uint32_t)((2 * seg) ^ (c & 7)) << 4), o[0], o[1], o[2], o[3]);
+    st_shared_v4(line + ((uint32_t)((2 * seg + 1) ^ (c & 7)) << 4), o[4], o[5], o[6], o[7]);
 }
 
 // Persistent CTAs walk 128x128 tiles (grid-stride).  Thread 0 keeps the next
 // tile's TMA load in flight; each warp releases a stage on its own (an mbarrier
-// arrival), so warps never wait for one another except where a tile needs a
-// cross-warp reduction (128x128 blocks, 128x1 column blocks).  Row pass: thread t holds the 16-byte chunk column j = t % 16 of
+// arrival).  Row-wise only, warps never wait for one another except where a
+// tile needs a cross-warp reduction (128x128 blocks); with the column-wise copy
+// the CTA works in lock step (the codes are staged in the stage all warps read).
+// Row pass: thread t holds the 16-byte chunk column j = t % 16 of
 // rows t/16 + 16 i, i = 0..7.  Column pass: warp w covers column pairs
 // lane + 32 (w & 1) over the 32-row segment w / 2.
 // The tile loop (shared by the cast kernel and the fused current-scaling kernel).  For
 // per-tensor scaling `s_given` is the scale; block granularities compute their own.
 template <int GRAN, int FMT>
-__device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const QuantArgs& a, float s_given) {
+__device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const QuantArgs& a, float s_given) {
+    const CUtensorMap* tmX = &maps->x;
     extern __shared__ uint8_t smem_raw[];
     QuantSmem& S = *reinterpret_cast<QuantSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -198,10 +214,9 @@ __device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const Qua
     const int rsub = tid >> 4;
     const int64_t n_my = (a.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
 
-    // tiles that need a block-wide reduction keep the CTA in lock step (MX column scales: the four
-    // 32-row segments of a column come from four warps and leave as one 4-byte store)
+    // tiles that need a block-wide reduction, and the staged column-wise copy, keep the CTA in lock step
     constexpr bool kMX = GRAN == FP8_SCALE_MX_1x32 || GRAN == FP8_SCALE_MX_1x32_OCP;
-    const bool lockstep = GRAN == FP8_SCALE_BLOCK_128x128 || ((GRAN == FP8_SCALE_BLOCK_1x128 || kMX) && a.do_col);
+    const bool lockstep = GRAN == FP8_SCALE_BLOCK_128x128 || a.do_col;
     if (tid == 0) {
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(smem_u32(&S.full[s]), 1);
@@ -239,9 +254,11 @@ __device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const Qua
 
     for (int64_t i = 0; i < n_my; ++i) {
         if (tid == 0 && i >= 1 && i + 1 < n_my) {
-            // stage (i+1) % 2 held tile i-1: wait until every warp has released it, then refill
+            // stage (i+1) % 2 held tile i-1: wait until every warp has released it and the TMA store
+            // of its column-wise codes has read it, then refill
             const int64_t u = i - 1;
             if (mbar_wait_bounded(smem_u32(&S.empty[u % kQStages]), (uint32_t)((u / kQStages) & 1), &S.abort_flag)) {
+                if (a.do_col) bulk_wait_read_all();
                 issue(i + 1);
                 issued = i + 2;
             }
@@ -344,7 +361,6 @@ __device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const Qua
 
             uint32_t sA, sB;
             const int64_t ca = c0 + 2 * cp, cb = ca + 1;
-            const int64_t row0 = r0 + 32 * seg;
             if constexpr (GRAN == FP8_SCALE_TENSOR) {
                 sA = sB = s2_tensor;
             } else if constexpr (GRAN == FP8_SCALE_BLOCK_128x128) {
@@ -387,26 +403,30 @@ __device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const Qua
                     if (cb < a.cols) sf[cb * nb + r0 / kTile] = pow2_exact(-eB);
                 }
             }
-            uint32_t o[8];
+            uint32_t o[8], oB[8];
             if (GRAN == FP8_SCALE_TENSOR && !pow2_tensor) {
-                if (ca < a.cols) {
-                    encode_column32_f32<FMT, 0>(w, s_tensor, o);
-                    store_col32(a.q_col, ca, a.rows, row0, o);
-                }
-                if (cb < a.cols) {
-                    encode_column32_f32<FMT, 1>(w, s_tensor, o);
-                    store_col32(a.q_col, cb, a.rows, row0, o);
-                }
+                encode_column32_f32<FMT, 0>(w, s_tensor, o);
+                encode_column32_f32<FMT, 1>(w, s_tensor, oB);
             } else {
-                uint32_t oB[8];
                 encode_column_pair32<FMT>(w, (sA & 0xFFFFu) | (sB & 0xFFFF0000u), o, oB);
-                if (ca < a.cols) store_col32(a.q_col, ca, a.rows, row0, o);
-                if (cb < a.cols) store_col32(a.q_col, cb, a.rows, row0, oB);
+            }
+            // every warp has read the tile (row pass and column loads; the block granularities' barrier
+            // above already says so): the codes go into its stage and leave as one TMA store, which clips
+            // the rows and columns past the tensor's edge
+            if constexpr (!(kMX || GRAN == FP8_SCALE_BLOCK_1x128)) __syncthreads();
+            stage_col32(smem_u32(T), 2 * cp, seg, o);
+            stage_col32(smem_u32(T), 2 * cp + 1, seg, oB);
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                tma_store_2d(&maps->qc, smem_u32(T), (int)r0, (int)c0);
+                bulk_commit();
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&S.empty[st]));  // this warp is done with the stage
     }
+    if (tid == 0 && a.do_col) bulk_wait_all();  // the column-wise stores complete before the CTA exits
 
     __syncthreads();
     if (S.abort_flag) {
@@ -436,8 +456,8 @@ __device__ __forceinline__ void quantize_tiles(const CUtensorMap* tmX, const Qua
 }
 
 template <int GRAN, int FMT>
-__global__ void __launch_bounds__(kThreads, 3) quantize_tile_kernel(const __grid_constant__ CUtensorMap tmX, QuantArgs a) {
-    quantize_tiles<GRAN, FMT>(&tmX, a, GRAN == FP8_SCALE_TENSOR ? *a.scale : 1.0f);
+__global__ void __launch_bounds__(kThreads, 3) quantize_tile_kernel(const __grid_constant__ QuantMaps maps, QuantArgs a) {
+    quantize_tiles<GRAN, FMT>(&maps, a, GRAN == FP8_SCALE_TENSOR ? *a.scale : 1.0f);
 }
 
 // ------------------------------------------------- fused current scaling
@@ -469,7 +489,7 @@ struct CurrentOut {
 
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 3)
-    quantize_current_kernel(const __grid_constant__ CUtensorMap tmX, QuantArgs a, const uint16_t* x, int64_t ld,
+    quantize_current_kernel(const __grid_constant__ QuantMaps maps, QuantArgs a, const uint16_t* x, int64_t ld,
                             CurrentOut out, CurrentWorkspace* ws) {
     __shared__ uint32_t red[kThreads / 32];
     __shared__ float s_scale;
@@ -543,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (s_abort) return;
 
     // phase 2: the cast
-    quantize_tiles<FP8_SCALE_TENSOR, FMT>(&tmX, a, s_scale);
+    quantize_tiles<FP8_SCALE_TENSOR, FMT>(&maps, a, s_scale);
 }
 
 // Standalone amax: grid-stride over 16-byte chunks, four loads in flight per thread.
@@ -645,7 +665,7 @@ PFN_cuTensorMapEncodeTiled_v12000 q_encode_fn() {
 }
 
 template <int GRAN, int FMT>
-fp8_status launch_quant(const CUtensorMap& tm, const QuantArgs& a, cudaStream_t st) {
+fp8_status launch_quant(const QuantMaps& tm, const QuantArgs& a, cudaStream_t st) {
     auto k = quantize_tile_kernel<GRAN, FMT>;
     const size_t smem = sizeof(QuantSmem) + 1024;
     static std::mutex mu;
@@ -735,6 +755,27 @@ fp8_status make_x_map(const void* x, int64_t rows, int64_t cols, int64_t ld, CUt
     return FP8_OK;
 }
 
+// The launch's maps: x as above; the column-wise output u8 [cols x rows] (rows a multiple of 16, base
+// 16-byte aligned, both checked by the API) in 128 (rows) x 128 (columns) boxes with the 128B swizzle
+// the kernel stages them in.  Without a column-wise output the second map is left zero and unused.
+fp8_status make_maps(const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q_col, QuantMaps* m) {
+    fp8_status s = make_x_map(x, rows, cols, ld, &m->x);
+    if (s != FP8_OK) return s;
+    memset(&m->qc, 0, sizeof(m->qc));
+    if (!q_col) return FP8_OK;
+    auto fn = q_encode_fn();
+    FP8_REQUIRE(fn != nullptr, FP8_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)rows, (cuuint64_t)cols};
+    cuuint64_t strides[1] = {(cuuint64_t)rows};
+    cuuint32_t box[2] = {(cuuint32_t)kTile, (cuuint32_t)kTile};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(&m->qc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q_col, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    FP8_REQUIRE(r == CUDA_SUCCESS, FP8_ERR_CUDA, "cuTensorMapEncodeTiled (column-wise output) failed (%d)", (int)r);
+    return FP8_OK;
+}
+
 __global__ void current_empty_kernel(CurrentOut out) {
     if (out.amax) *out.amax = 0.0f;
     if (out.bias) *out.bias = 0;
@@ -743,7 +784,7 @@ __global__ void current_empty_kernel(CurrentOut out) {
 }
 
 template <int FMT>
-fp8_status launch_current(const CUtensorMap& tm, const QuantArgs& a, const void* x, int64_t ld, const CurrentOut& out,
+fp8_status launch_current(const QuantMaps& tm, const QuantArgs& a, const void* x, int64_t ld, const CurrentOut& out,
                           void* workspace, cudaStream_t st) {
     auto k = quantize_current_kernel<FMT>;
     const size_t smem = sizeof(QuantSmem) + 1024;
@@ -773,7 +814,7 @@ fp8_status launch_current(const CUtensorMap& tm, const QuantArgs& a, const void*
     if (grid > a.ntiles) grid = a.ntiles;
     if (grid > kCurrentMaxCtas) grid = kCurrentMaxCtas;
     if (grid < 1) grid = 1;
-    CUtensorMap tm_arg = tm;
+    QuantMaps tm_arg = tm;
     QuantArgs a_arg = a;
     const uint16_t* x_arg = static_cast<const uint16_t*>(x);
     int64_t ld_arg = ld;
@@ -811,8 +852,8 @@ QuantArgs quant_args(int64_t rows, int64_t cols, int margin, const float* scale,
 fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int gran, int margin,
                            const float* scale, uint8_t* q_row, uint8_t* q_col, void* sf_row, void* sf_col,
                            float* amax, cudaStream_t st) {
-    CUtensorMap tm;
-    fp8_status s = make_x_map(x, rows, cols, ld, &tm);
+    QuantMaps tm;
+    fp8_status s = make_maps(x, rows, cols, ld, q_col, &tm);
     if (s != FP8_OK) return s;
     const QuantArgs a = quant_args(rows, cols, margin, scale, q_row, q_col, sf_row, sf_col, amax);
 #define FP8Q_QDISPATCH(G)                                                         \
@@ -837,8 +878,8 @@ fp8_status launch_quantize_current(const void* x, int64_t rows, int64_t cols, in
         current_empty_kernel<<<1, 1, 0, st>>>(out);
         return check_launch("current-scaling kernel launch");
     }
-    CUtensorMap tm;
-    fp8_status s = make_x_map(x, rows, cols, ld, &tm);
+    QuantMaps tm;
+    fp8_status s = make_maps(x, rows, cols, ld, q_col, &tm);
     if (s != FP8_OK) return s;
     QuantArgs a = quant_args(rows, cols, margin, nullptr, q_row, q_col, nullptr, nullptr, nullptr);
     a.status = status;
@@ -892,7 +933,7 @@ fp8_status noalloc_scratch(void** out) {
 }
 
 template <int FMT>
-fp8_status launch_current_noalloc(const CUtensorMap& tm, const QuantArgs& a, const void* x, int64_t ld,
+fp8_status launch_current_noalloc(const QuantMaps& tm, const QuantArgs& a, const void* x, int64_t ld,
                                   const CurrentOut& out, void* scratch, cudaStream_t st) {
     auto k = quantize_current_kernel<FMT>;
     const size_t smem = sizeof(QuantSmem) + 1024;
@@ -925,7 +966,7 @@ fp8_status launch_current_noalloc(const CUtensorMap& tm, const QuantArgs& a, con
                 (long long)need, (long long)grid, kNoAllocScratchBytes, (kNoAllocScratchBytes - kCurrentWsHeader) / 4);
     cudaError_t e = cudaMemsetAsync(scratch, 0, kCurrentWsHeader, st);
     FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaMemsetAsync(scratch header): %s", cudaGetErrorString(e));
-    CUtensorMap tm_arg = tm;
+    QuantMaps tm_arg = tm;
     QuantArgs a_arg = a;
     const uint16_t* x_arg = static_cast<const uint16_t*>(x);
     int64_t ld_arg = ld;
@@ -951,8 +992,8 @@ fp8_status launch_quantize_current_noalloc(const void* x, int64_t rows, int64_t 
     void* scratch = nullptr;
     fp8_status s = noalloc_scratch(&scratch);
     if (s != FP8_OK) return s;
-    CUtensorMap tm;
-    s = make_x_map(x, rows, cols, ld, &tm);
+    QuantMaps tm;
+    s = make_maps(x, rows, cols, ld, q_col, &tm);
     if (s != FP8_OK) return s;
     QuantArgs a = quant_args(rows, cols, margin, nullptr, q_row, q_col, nullptr, nullptr, nullptr);
     a.status = status;
