@@ -220,6 +220,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint3
         : "memory");
 }
 
+// Same, with an L2 cache policy (from createpolicy) attached to the load.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* map, uint32_t bar, int x, int y,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], "
+        "[%4], %5;" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // TMA store of a shared-memory box to global memory (bulk-group completion).  Elements outside the
 // tensor's extent are not written.  The generic-proxy writes that filled the box must be made
 // visible to the async proxy first (fence_proxy_async_smem by every writer, then a barrier).

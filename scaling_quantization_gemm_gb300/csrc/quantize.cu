@@ -226,12 +226,19 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
         mbar_fence_init();
     }
     __syncthreads();
+    // x is read once.  Per-tensor casts mark its lines evict-first in L2, which leaves L2 to the
+    // outputs (measured: row+col per-tensor cast 6 % faster); the block granularities measured
+    // slower with the hint and load without it.
+    const uint64_t policy = GRAN == FP8_SCALE_TENSOR && tid == 0 ? l2_policy_evict_first() : 0;
     auto issue = [&](int64_t i) {  // TMA load of this CTA's i-th tile into stage i % kQStages
         const int64_t tile = blockIdx.x + i * gridDim.x;
         const int st = (int)(i % kQStages);
+        const int x0 = (int)((tile % a.tiles_c) * kTile), y0 = (int)((tile / a.tiles_c) * kTile);
         mbar_arrive_expect_tx(smem_u32(&S.full[st]), kTile * kTile * 2);
-        tma_load_2d(smem_u32(S.tile[st]), tmX, smem_u32(&S.full[st]), (int)((tile % a.tiles_c) * kTile),
-                    (int)((tile / a.tiles_c) * kTile));
+        if constexpr (GRAN == FP8_SCALE_TENSOR)
+            tma_load_2d_hint(smem_u32(S.tile[st]), tmX, smem_u32(&S.full[st]), x0, y0, policy);
+        else
+            tma_load_2d(smem_u32(S.tile[st]), tmX, smem_u32(&S.full[st]), x0, y0);
     };
     int64_t issued = 0;  // meaningful in thread 0
     if (tid == 0) {
