@@ -245,6 +245,27 @@ FP8Q_API fp8_status fp8_quantize(const void *x, int64_t rows, int64_t cols, int6
                         void *sf_row, void *sf_col, float *amax, void *stream);
 
 /*
+ * fp8_quantize_f32 -- the per-tensor scaled cast of an fp32 tensor.
+ * Source: the scaling step that precedes the FP8 cast ("Training and
+ * inference of large language models using 8-bit floating point", "Proposed
+ * method"), for tensors held in fp32 (master weights, fp32 GEMM outputs).
+ *
+ *   q[i] = RNE_saturate_fmt(fl32(x[i] * s)),  s = *scale, or 1 when scale is NULL.
+ *
+ *   x       device, fp32[n], dense, 16-byte aligned.
+ *   n       element count; 0 is a no-op.
+ *   scale   device fp32 (any value; 2^e from fp8_compute_scale in the usual
+ *           case, when the product is exact) or NULL.
+ *   q       device u8[n], 8-byte aligned.
+ *   amax    device fp32 or NULL: if given, max|x| is accumulated into it
+ *           (a NaN element makes it NaN), as for fp8_amax.
+ * A NaN element casts to a NaN code; +-Inf and products beyond fmax saturate
+ * to +-fmax.
+ */
+FP8Q_API fp8_status fp8_quantize_f32(const float *x, int64_t n, fp8_format fmt, const float *scale, uint8_t *q,
+                                     float *amax, void *stream);
+
+/*
  * fp8_quantize_current -- per-tensor current scaling and the cast, in one launch.
  * Source: FP8-AMAX scaling from the amax of the tensor being cast, the
  * compute_bias rule, then the scaled cast ("Training and inference of large

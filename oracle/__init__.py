@@ -18,7 +18,8 @@ What each function computes, and the passage it follows, is stated in
   behind options (the OCP MX rule for 1x32 blocks, and s = fmax / amax).
 * ``quantize_tensor`` / ``quantize_block`` -- Encode(x * 2^e), per tensor or per
   block ("Per-Tensor and Per-Block Scaling Strategies for Effective FP8
-  Training", "Key Questions Answered").
+  Training", "Key Questions Answered"); ``quantize_f32`` / ``amax_f32`` -- the
+  per-tensor cast and amax of an fp32 array.
 * ``history_update`` -- delayed scaling from an amax window (same page).
 * ``gemm_sample`` / ``gemm_full`` -- fp64 product of the dequantised operands.
 * ``gemm_quantize_bracket`` -- the FP8 codes a GEMM whose output is cast for the
@@ -85,6 +86,9 @@ def lib() -> ctypes.CDLL:
             L.fp8o_amax.restype = f32
             L.fp8o_amax.argtypes = [vp, i64, i64, i64]
             L.fp8o_quantize_tensor.argtypes = [vp, i64, i64, i64, i32, f32, vp, vp]
+            L.fp8o_quantize_f32.argtypes = [vp, i64, i32, f32, vp]
+            L.fp8o_amax_f32.restype = f32
+            L.fp8o_amax_f32.argtypes = [vp, i64]
             L.fp8o_quantize_block.restype = i32
             L.fp8o_quantize_block.argtypes = [vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp]
             L.fp8o_history_update.restype = i32
@@ -183,6 +187,20 @@ def amax(x_bf16: np.ndarray) -> np.float32:
 
 
 # ------------------------------------------------------------- quantise
+
+def quantize_f32(x: np.ndarray, fmt: int, scale: float = 1.0) -> np.ndarray:
+    """Per-tensor cast of an fp32 array: Encode(fl32(x * scale)), same shape, uint8 codes."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    q = np.empty(x.shape, dtype=np.uint8)
+    lib().fp8o_quantize_f32(_p(x), x.size, fmt, float(np.float32(scale)), _p(q))
+    return q
+
+
+def amax_f32(x: np.ndarray) -> np.float32:
+    """max |x| of an fp32 array (NaN if any element is NaN)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return np.float32(lib().fp8o_amax_f32(_p(x), x.size))
+
 
 def quantize_tensor(x_bf16: np.ndarray, fmt: int, scale: float, row: bool = True, col: bool = False):
     """Per-tensor cast with scale s: returns (q_row or None, q_col or None)."""

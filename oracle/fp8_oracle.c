@@ -244,6 +244,29 @@ void fp8o_quantize_tensor(const uint16_t *x, int64_t rows, int64_t cols, int64_t
         }
 }
 
+/* Per-tensor cast of an fp32 array x[n] with scale s: q[i] = Encode(x[i] * s),
+ * the product one fp32 multiplication (the same "scale, then cast" step, for
+ * tensors held in fp32).  Its amax is max |x[i]|, NaN if any element is NaN. */
+void fp8o_quantize_f32(const float *x, int64_t n, int fmt, float s, uint8_t *q)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        float p = x[i] * s;
+        q[i] = (uint8_t)fp8o_encode(p, fmt);
+    }
+}
+
+float fp8o_amax_f32(const float *x, int64_t n)
+{
+    float m = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(x[i]);
+        if (isnan(a)) return a;
+        if (a > m) m = a;
+    }
+    return m;
+}
+
 /* Block-scaled cast of the rows x cols matrix v(i,j) = x[i*rs + j*cs] with
  * br x bc blocks (a partial block at an edge covers the elements that exist).
  * Each block b: amax_b, e_b = compute_bias(amax_b, margin), q = Encode(v 2^e_b).

@@ -33,7 +33,8 @@ STATUS_NONFINITE_AMAX, STATUS_TIMEOUT, STATUS_BAD_BLOCK_SCALE = 1, 2, 4
 
 # every entry point declared in include/fp8q.h
 ENTRY_POINTS = ("fp8_amax", "fp8_compute_scale", "fp8_compute_scale_ratio", "fp8_amax_history_update",
-                "fp8_set_bias", "fp8_cast_stats", "fp8_quantize", "fp8_quantize_current", "fp8_quantize_current_noalloc",
+                "fp8_set_bias", "fp8_cast_stats", "fp8_quantize", "fp8_quantize_f32", "fp8_quantize_current",
+                "fp8_quantize_current_noalloc",
                 "fp8_scaled_gemm", "fp8_scaled_gemm_quantize", "fp8_status_string", "fp8_last_error_detail")
 QUANTIZE_CURRENT_WORKSPACE_BYTES = 4096  # FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES
 
@@ -64,6 +65,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_compute_scale_ratio": [vp, i32, vp, vp, vp, vp],
                 "fp8_amax_history_update": [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp],
                 "fp8_quantize": [vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp],
+                "fp8_quantize_f32": [vp, i64, i32, vp, vp, vp, vp],
                 "fp8_set_bias": [i32, vp, vp, vp, vp],
                 "fp8_cast_stats": [vp, i64, i64, i64, i32, vp, i32, vp, vp, vp],
                 "fp8_quantize_current": [vp, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp],
@@ -166,6 +168,15 @@ def fp8_quantize(x: torch.Tensor, fmt: int, gran: int, margin: int = 0, scale: P
                                               _p(q_col), _p(sf_row), _p(sf_col), _p(amax), _stream(stream)))
 
 
+def fp8_quantize_f32(x: torch.Tensor, fmt: int, q: torch.Tensor, scale: Ptr = None, amax: Ptr = None,
+                     stream=None) -> None:
+    """q = RNE_sat(fl32(x * scale)) for a dense fp32 tensor x (any shape) into u8 q of the same size."""
+    if x.dtype != torch.float32 or not x.is_contiguous() or q.dtype != torch.uint8 or q.numel() != x.numel():
+        raise ValueError("expected a dense float32 x and a uint8 q with as many elements")
+    _check("fp8_quantize_f32", lib().fp8_quantize_f32(_p(x), x.numel(), fmt, _p(scale), _p(q), _p(amax),
+                                                      _stream(stream)))
+
+
 def current_workspace(device=None) -> torch.Tensor:
     """A zeroed workspace for fp8_quantize_current (one per stream that calls it)."""
     return torch.zeros(QUANTIZE_CURRENT_WORKSPACE_BYTES, dtype=torch.uint8, device=device or "cuda")
@@ -225,7 +236,7 @@ def fp8_scaled_gemm_quantize(op: int, A: torch.Tensor, fa: int, sfa: Ptr, B: tor
 __all__ = ["lib", "FP8Error", "status_name", "fp8_amax", "fp8_compute_scale", "fp8_compute_scale_ratio",
            "fp8_amax_history_update",
            "fp8_set_bias", "fp8_cast_stats",
-           "fp8_quantize", "fp8_quantize_current", "fp8_quantize_current_noalloc",
+           "fp8_quantize", "fp8_quantize_f32", "fp8_quantize_current", "fp8_quantize_current_noalloc",
            "current_workspace", "fp8_scaled_gemm", "fp8_scaled_gemm_quantize", "ENTRY_POINTS",
            "QUANTIZE_CURRENT_WORKSPACE_BYTES", "LIB_PATH", "E4M3", "E5M2", "TENSOR", "BLOCK_1x128",
            "BLOCK_128x128", "MX_1x32", "MX_1x32_OCP", "FPROP", "DGRAD", "WGRAD", "OUT_F32", "OUT_BF16"]

@@ -32,6 +32,8 @@ fp8_status launch_quantize_current_noalloc(const void* x, int64_t rows, int64_t 
                                            int margin, uint8_t* q_row, uint8_t* q_col, float* amax, int32_t* bias,
                                            float* scale, float* scale_inv, int32_t* status, cudaStream_t st);
 fp8_status launch_set_bias(int e, int32_t* bias, float* scale, float* scale_inv, cudaStream_t st);
+fp8_status launch_quantize_f32(const float* x, int64_t n, int fmt, const float* scale, uint8_t* q, float* amax,
+                               cudaStream_t st);
 fp8_status launch_cast_stats(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, const float* scales,
                              int n, uint64_t* saturated, uint64_t* underflow, cudaStream_t st);
 fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int gran, int margin,
@@ -222,6 +224,20 @@ fp8_status fp8_cast_stats(const void* x, int64_t rows, int64_t cols, int64_t ld,
                 "scales must be 4-byte and the counters 8-byte aligned");
     if (rows == 0 || cols == 0) return FP8_OK;
     return launch_cast_stats(x, rows, cols, ld, fmt, scales, n, saturated, underflow, as_stream(stream));
+}
+
+fp8_status fp8_quantize_f32(const float* x, int64_t n, fp8_format fmt, const float* scale, uint8_t* q, float* amax,
+                            void* stream) {
+    g_detail[0] = 0;
+    FP8_REQUIRE(n >= 0, FP8_ERR_INVALID_ARG, "negative size");
+    FP8_REQUIRE(valid_fmt(fmt), FP8_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
+    if (n == 0) return FP8_OK;
+    FP8_REQUIRE(x && q, FP8_ERR_INVALID_ARG, "x and q are required");
+    FP8_REQUIRE(aligned(x, 16), FP8_ERR_UNSUPPORTED, "x must be 16-byte aligned");
+    FP8_REQUIRE(aligned(q, 8), FP8_ERR_UNSUPPORTED, "q must be 8-byte aligned");
+    FP8_REQUIRE((!scale || aligned(scale, 4)) && (!amax || aligned(amax, 4)), FP8_ERR_INVALID_ARG,
+                "scale and amax must be 4-byte aligned");
+    return launch_quantize_f32(x, n, fmt, scale, q, amax, as_stream(stream));
 }
 
 fp8_status fp8_scaled_gemm(fp8_gemm_op op, int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,

@@ -573,6 +573,38 @@ __global__ void __launch_bounds__(kThreads, 3)
     quantize_tiles<FP8_SCALE_TENSOR, FMT>(&maps, a, s_scale);
 }
 
+// Per-tensor scaled cast of an fp32 tensor: q = Encode(fl32(x s)), grid-stride over 8-element
+// chunks (two 16-byte loads, one 8-byte store); the n % 8 tail is cast by the first threads of
+// CTA 0.  The fused amax takes the largest |x| bit pattern, so a NaN wins.
+template <int FMT>
+__global__ void __launch_bounds__(256) cast_f32_kernel(const float* x, int64_t n, const float* scale, uint8_t* q,
+                                                       float* amax) {
+    const float s = scale ? *scale : 1.0f;
+    const int64_t n8 = n >> 3;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    uint32_t m = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        const uint4 a = ld_stream_v4(x + 8 * i), b = ld_stream_v4(x + 8 * i + 4);
+        const uint32_t lo = cvt_fp8x2<FMT>(__fmul_rn(__uint_as_float(a.x), s), __fmul_rn(__uint_as_float(a.y), s)) |
+                            (cvt_fp8x2<FMT>(__fmul_rn(__uint_as_float(a.z), s), __fmul_rn(__uint_as_float(a.w), s)) << 16);
+        const uint32_t hi = cvt_fp8x2<FMT>(__fmul_rn(__uint_as_float(b.x), s), __fmul_rn(__uint_as_float(b.y), s)) |
+                            (cvt_fp8x2<FMT>(__fmul_rn(__uint_as_float(b.z), s), __fmul_rn(__uint_as_float(b.w), s)) << 16);
+        *reinterpret_cast<uint2*>(q + 8 * i) = make_uint2(lo, hi);
+        m = max(m, max(max(max(a.x & 0x7FFFFFFFu, a.y & 0x7FFFFFFFu), max(a.z & 0x7FFFFFFFu, a.w & 0x7FFFFFFFu)),
+                       max(max(b.x & 0x7FFFFFFFu, b.y & 0x7FFFFFFFu), max(b.z & 0x7FFFFFFFu, b.w & 0x7FFFFFFFu))));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n & 7)) {
+        const int64_t i = 8 * n8 + threadIdx.x;
+        const uint32_t u = __float_as_uint(x[i]);
+        q[i] = (uint8_t)cvt_fp8x2<FMT>(__fmul_rn(__uint_as_float(u), s), 0.0f);
+        m = max(m, u & 0x7FFFFFFFu);
+    }
+    if (amax) {
+        m = __reduce_max_sync(0xffffffffu, m);
+        if ((threadIdx.x & 31) == 0 && m) atomicMax(reinterpret_cast<unsigned int*>(amax), m);
+    }
+}
+
 // Standalone amax: grid-stride over 16-byte chunks, four loads in flight per thread.
 __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* amax) {
     const int64_t cpr = cols >> 3;
@@ -724,6 +756,19 @@ fp8_status launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, fl
     if (grid < 1) grid = 1;
     amax_kernel<<<(int)grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), rows, cols, ld, amax);
     return check_launch("amax kernel launch");
+}
+
+fp8_status launch_quantize_f32(const float* x, int64_t n, int fmt, const float* scale, uint8_t* q, float* amax,
+                               cudaStream_t st) {
+    int64_t grid = ((n >> 3) + 255) / 256;
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    if (fmt == FP8_E4M3)
+        cast_f32_kernel<FP8_E4M3><<<(int)grid, 256, 0, st>>>(x, n, scale, q, amax);
+    else
+        cast_f32_kernel<FP8_E5M2><<<(int)grid, 256, 0, st>>>(x, n, scale, q, amax);
+    return check_launch("fp32 cast kernel launch");
 }
 
 fp8_status launch_compute_scale(const float* amax, int fmt, int margin, int32_t* bias, float* scale,

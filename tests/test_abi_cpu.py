@@ -186,3 +186,15 @@ def test_compute_scale_ratio_validation(L):
     assert L.fp8_compute_scale_ratio(FAKE, 0, None, None, None, None) == 1
     q = L.fp8_quantize
     assert q(FAKE, 32, 32, 32, 0, 5, 0, None, FAKE, None, FAKE, None, None, None) == 1  # granularity 5 unknown
+
+
+def test_quantize_f32_validation(L):
+    f = L.fp8_quantize_f32
+    assert f(None, 0, 0, None, None, None, None) == 0          # empty: no-op, nothing required
+    assert f(FAKE, -1, 0, None, FAKE, None, None) == 1         # negative size
+    assert f(FAKE, 8, 2, None, FAKE, None, None) == 1          # unknown format
+    assert f(None, 8, 0, None, FAKE, None, None) == 1          # x required
+    assert f(FAKE, 8, 0, None, None, None, None) == 1          # q required
+    assert f(FAKE + 4, 8, 0, None, FAKE, None, None) == 2      # x not 16-byte aligned
+    assert f(FAKE, 8, 0, None, FAKE + 2, None, None) == 2      # q not 8-byte aligned
+    assert f(FAKE, 8, 0, FAKE + 1, FAKE, None, None) == 1      # scale misaligned
