@@ -259,3 +259,31 @@ def test_calls_run_on_the_callers_stream(q):
     side.synchronize()
     assert host(amax)[0] == amax_ref
     assert_codes_equal(host(out), oracle.quantize_tensor(xb, 0, oracle.scale_triple(amax_ref, 0)[1])[0], 0)
+
+
+@pytest.mark.parametrize("gran", [0, 1, 2, 3])
+@pytest.mark.parametrize("shape", [(48, 136), (272, 520)])
+def test_quantize_col_bounds_and_offset(q, gran, shape):
+    """The column-wise copy written at a 16-byte (not 128-byte) aligned offset inside a larger buffer:
+    the codes match the oracle and no byte before or after the [cols x rows] block changes (the tile
+    stores are clipped at the tensor's edge)."""
+    r, c = shape
+    x_bits = wl.random_bf16(300 + r + gran, r, c, "normal", 2.0)
+    x = dev_bf16(x_bits)
+    off, pad = 48, 4096
+    buf = torch.full((off + c * r + pad,), 0x5A, dtype=torch.uint8, device="cuda")
+    qc = buf[off:off + c * r].view(c, r)
+    srow, scol = oracle.scale_shapes(r, c, gran) if gran else ((0, 0), (0, 0))
+    sdt = torch.uint8 if gran == q.MX_1x32 else torch.float32
+    sc = torch.empty(scol, dtype=sdt, device="cuda") if gran else None
+    if gran == 0:
+        s = oracle.scale_triple(oracle.amax(x_bits), 0)[1]
+        q.fp8_quantize(x, 0, gran, 0, scale=torch.tensor([float(s)], device="cuda"), q_col=qc)
+        _, rc = oracle.quantize_tensor(x_bits, 0, s, row=False, col=True)
+    else:
+        q.fp8_quantize(x, 0, gran, 0, q_col=qc, sf_col=sc)
+        _, _, rc, rsc, _ = oracle.quantize_block(x_bits, 0, gran, 0, row=False, col=True)
+        assert np.array_equal(host(sc), rsc)
+    assert_codes_equal(host(qc), rc, 0, "col")
+    b = host(buf)
+    assert (b[:off] == 0x5A).all() and (b[off + c * r:] == 0x5A).all()
