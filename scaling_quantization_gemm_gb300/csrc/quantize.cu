@@ -9,16 +9,16 @@
 // Effective FP8 Training", "Key Questions Answered").
 //
 // All of it is HBM-bound.  The cast kernel streams 128x128 bf16 tiles through
-// a two-deep TMA ring per CTA, three CTAs per SM (up to six tile loads in
-// flight per SM), computes block maxima in registers (warp shuffles), writes
-// the row-wise codes, and reads the same tile down its columns for the
-// transposed column-wise codes, so one HBM read feeds both outputs.  The
-// column-wise codes of a tile are staged (128B-swizzled) in the tile's own
-// shared-memory stage once every warp has read it, and leave as one TMA store
-// of whole 128-byte lines; the stage is refilled after that store has read it.  The fused
-// amax is reduced per warp, per CTA, then one atomic per CTA.  Current scaling
-// runs the amax pass and the cast in one cooperative launch with a grid
-// barrier between them.
+// a two-deep TMA ring per CTA, three CTAs per SM (each CTA works on one tile
+// while the next one loads), computes block maxima in registers (warp
+// shuffles), writes the row-wise codes, and reads the same tile down its
+// columns for the transposed column-wise codes, so one HBM read feeds both
+// outputs.  The column-wise codes of a tile are staged (128B-swizzled) in the
+// tile's own shared-memory stage once every warp has read it, and leave as one
+// TMA store of whole 128-byte lines; the stage is refilled after that store has
+// read it.  The fused amax is reduced per warp, per CTA, then one atomic per
+// CTA.  Current scaling runs the amax pass and the cast in one cooperative
+// launch with a grid barrier between them.
 #include <cudaTypedefs.h>
 
 #include <cstdarg>
@@ -34,7 +34,7 @@ namespace {
 
 constexpr int kTile = 128;     // tile is kTile x kTile bf16 elements (32 KB)
 constexpr int kThreads = 256;
-constexpr int kQStages = 2;    // TMA ring depth (3 CTAs per SM: up to 6 tiles in flight per SM)
+constexpr int kQStages = 2;    // TMA ring depth (3 CTAs per SM)
 
 struct QuantArgs {
     int64_t rows, cols;
