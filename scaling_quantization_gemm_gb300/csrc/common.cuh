@@ -36,6 +36,8 @@ inline fp8_status check_launch(const char* what) {
 }
 
 int device_sm_count();
+// Resident CTAs per SM of `kernel` on the current device (cached per kernel and device; no heap).
+fp8_status resident_ctas(const void* kernel, int threads, size_t smem, int* occ);
 
 // ------------------------------------------------------------ bias / scales
 

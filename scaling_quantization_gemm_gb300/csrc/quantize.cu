@@ -21,6 +21,7 @@
 // launch with a grid barrier between them.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -707,25 +708,9 @@ template <int GRAN, int FMT>
 fp8_status launch_quant(const QuantMaps& tm, const QuantArgs& a, cudaStream_t st) {
     auto k = quantize_tile_kernel<GRAN, FMT>;
     const size_t smem = sizeof(QuantSmem) + 1024;
-    static std::mutex mu;
-    static int occ_dev[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int occ;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev < 0 || dev >= 64 || occ_dev[dev] == 0) {
-            cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            int o = 0;
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k, kThreads, smem);
-            occ = o > 0 ? o : 1;
-            if (dev >= 0 && dev < 64) occ_dev[dev] = occ;
-        } else {
-            occ = occ_dev[dev];
-        }
-    }
+    int occ = 0;
+    fp8_status s = resident_ctas(reinterpret_cast<const void*>(k), kThreads, smem, &occ);
+    if (s != FP8_OK) return s;
     const int64_t cap = (int64_t)device_sm_count() * occ;
     const int grid = (int)(a.ntiles < cap ? a.ntiles : cap);
     k<<<grid, kThreads, smem, st>>>(tm, a);
@@ -736,15 +721,51 @@ fp8_status launch_quant(const QuantMaps& tm, const QuantArgs& a, cudaStream_t st
 
 // ------------------------------------------------------------------- host API
 
+// Resident CTAs per SM of `kernel` (`threads` threads, `smem` bytes of dynamic shared memory) on the
+// current device.  The first call for a kernel on a device raises its shared-memory limit and queries
+// the occupancy; the answer is kept in a fixed table (no heap allocation), so later calls, including
+// those made while a stream is being captured, make neither CUDA call.
+fp8_status resident_ctas(const void* kernel, int threads, size_t smem, int* occ) {
+    struct Entry {
+        const void* kernel;
+        int dev, occ;
+    };
+    constexpr int kEntries = 256;  // 12 cast and 8 statistics kernels per device
+    static std::mutex mu;
+    static Entry table[kEntries];
+    static int used = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (table[i].kernel == kernel && table[i].dev == dev) {
+            *occ = table[i].occ;
+            return FP8_OK;
+        }
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    int o = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, threads, smem);
+    FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+    FP8_REQUIRE(o > 0, FP8_ERR_CUDA, "a %d-thread CTA with %zu bytes of shared memory does not fit on an SM", threads,
+                smem);
+    if (used < kEntries) table[used++] = Entry{kernel, dev, o};
+    *occ = o;
+    return FP8_OK;
+}
+
 int device_sm_count() {
     int dev = 0;
     cudaGetDevice(&dev);
-    static int cache[64] = {0};
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    static std::atomic<int> cache[64];  // zero until the first query on that device
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (n <= 0) n = 1;
-    if (dev >= 0 && dev < 64) cache[dev] = n;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -840,26 +861,9 @@ fp8_status launch_current(const QuantMaps& tm, const QuantArgs& a, const void* x
                           void* workspace, cudaStream_t st) {
     auto k = quantize_current_kernel<FMT>;
     const size_t smem = sizeof(QuantSmem) + 1024;
-    static std::mutex mu;
-    static int occ_dev[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int occ;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev < 0 || dev >= 64 || occ_dev[dev] == 0) {
-            cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            int o = 0;
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k, kThreads, smem);
-            FP8_REQUIRE(o > 0, FP8_ERR_CUDA, "current-scaling kernel does not fit on an SM");
-            occ = o;
-            if (dev >= 0 && dev < 64) occ_dev[dev] = occ;
-        } else {
-            occ = occ_dev[dev];
-        }
-    }
+    int occ = 0;
+    fp8_status s = resident_ctas(reinterpret_cast<const void*>(k), kThreads, smem, &occ);
+    if (s != FP8_OK) return s;
     // every CTA must be resident at once (grid barrier): at most SMs x occupancy, and one
     // workspace slot per CTA
     int64_t grid = (int64_t)device_sm_count() * occ;
@@ -989,26 +993,9 @@ fp8_status launch_current_noalloc(const QuantMaps& tm, const QuantArgs& a, const
                                   const CurrentOut& out, void* scratch, cudaStream_t st) {
     auto k = quantize_current_kernel<FMT>;
     const size_t smem = sizeof(QuantSmem) + 1024;
-    static std::mutex mu;
-    static int occ_dev[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int occ;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev < 0 || dev >= 64 || occ_dev[dev] == 0) {
-            cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            int o = 0;
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k, kThreads, smem);
-            FP8_REQUIRE(o > 0, FP8_ERR_CUDA, "current-scaling kernel does not fit on an SM");
-            occ = o;
-            if (dev >= 0 && dev < 64) occ_dev[dev] = occ;
-        } else {
-            occ = occ_dev[dev];
-        }
-    }
+    int occ = 0;
+    fp8_status s = resident_ctas(reinterpret_cast<const void*>(k), kThreads, smem, &occ);
+    if (s != FP8_OK) return s;
     int64_t grid = (int64_t)device_sm_count() * occ;  // all CTAs resident at once (grid barrier)
     if (grid > a.ntiles) grid = a.ntiles;
     if (grid < 1) grid = 1;

@@ -14,9 +14,12 @@
 // The cast is monotone in |x|, so for each scale both sets are ranges of bf16
 // magnitudes: saturated iff |x| >= T_j, flushed iff 0 < |x| <= U_j.  Every CTA
 // finds T_j and U_j by bisection over the 2^15 magnitudes with the same fp32
-// product and conversion instruction the cast kernels use; the pass over x is
-// then two integer compares per element and scale (one 16-byte load per
-// thread per step, grid-stride).
+// product and conversion instruction the cast kernels use.  The pass over x
+// (one 16-byte load per thread per step, grid-stride) then compares the two
+// magnitudes of a 32-bit word with a threshold in one packed bf16x2 compare
+// (a NaN compares false) and adds the two 0xFFFF / 0 lane masks into packed
+// 16-bit counters that count down; flushed counts are |x| <= U_j less the
+// zeros, counted once per word.
 #include "common.cuh"
 
 namespace fp8q {
@@ -79,16 +82,42 @@ __device__ void thresholds(float s, uint32_t& T, uint32_t& U) {
     }
 }
 
+__device__ __forceinline__ uint32_t ge_mask2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t le_mask2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("set.le.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t eq_mask2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("set.eq.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// Lane-wise 16-bit add: adding a 0xFFFF mask lane takes one off that lane's count.
+__device__ __forceinline__ uint32_t add_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// Elements a packed count-down counter has seen in its two lanes.
+__device__ __forceinline__ uint32_t down_count(uint32_t c) {
+    return ((0x10000u - (c & 0xFFFFu)) & 0xFFFFu) + ((0x10000u - (c >> 16)) & 0xFFFFu);
+}
+
+// Both magnitudes of word w against every threshold pair (T2, U2: the bf16 threshold in both lanes).
 template <int NS>
-__device__ __forceinline__ void count2(uint32_t w, const uint32_t (&T)[NS], const uint32_t (&U)[NS],
-                                       uint32_t (&cs)[NS], uint32_t (&cu)[NS]) {
-    uint32_t m0 = w & 0x7FFFu, m1 = (w >> 16) & 0x7FFFu;
-    m0 = m0 > kInfMag ? 0u : m0;  // NaN counts in neither
-    m1 = m1 > kInfMag ? 0u : m1;
+__device__ __forceinline__ void count2(uint32_t w, const uint32_t (&T2)[NS], const uint32_t (&U2)[NS],
+                                       uint32_t (&ps)[NS], uint32_t (&pu)[NS], uint32_t& pz) {
+    const uint32_t m = w & 0x7FFF7FFFu;
+    pz = add_u16x2(pz, eq_mask2(m, 0u));
 #pragma unroll
     for (int j = 0; j < NS; ++j) {
-        cs[j] += (m0 >= T[j]) + (m1 >= T[j]);
-        cu[j] += (m0 - 1u < U[j]) + (m1 - 1u < U[j]);  // 0 wraps to 2^32 - 1: never counted
+        ps[j] = add_u16x2(ps[j], ge_mask2(m, T2[j]));
+        pu[j] = add_u16x2(pu[j], le_mask2(m, U2[j]));
     }
 }
 
@@ -106,24 +135,55 @@ __global__ void __launch_bounds__(kStatsThreads)
         sU[tid] = u;
     }
     __syncthreads();
-    uint32_t T[NS], U[NS], cs[NS], cu[NS];
+    uint32_t T2[NS], U2[NS], cs[NS], cu[NS], ps[NS], pu[NS], pz = 0, cz = 0;
 #pragma unroll
     for (int j = 0; j < NS; ++j) {
-        T[j] = sT[j];
-        U[j] = sU[j];
-        cs[j] = cu[j] = 0;
+        T2[j] = sT[j] * 0x10001u;
+        U2[j] = sU[j] * 0x10001u;
+        cs[j] = cu[j] = ps[j] = pu[j] = 0;
     }
+    // a packed lane counts at most 16 per step (four 16-byte chunks): fold the lanes into 32-bit counts
+    // every 2048 steps
+    auto fold = [&]() {
+#pragma unroll
+        for (int j = 0; j < NS; ++j) {
+            cs[j] += down_count(ps[j]);
+            cu[j] += down_count(pu[j]);
+            ps[j] = pu[j] = 0;
+        }
+        cz += down_count(pz);
+        pz = 0;
+    };
     const int64_t cpr = cols >> 3;
     const int64_t total = rows * cpr;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + tid; i < total; i += stride) {
-        const uint16_t* p = (ld == cols) ? x + i * 8 : x + (i / cpr) * ld + (i % cpr) * 8;
-        const uint4 v = ld_stream_v4(p);
-        count2<NS>(v.x, T, U, cs, cu);
-        count2<NS>(v.y, T, U, cs, cu);
-        count2<NS>(v.z, T, U, cs, cu);
-        count2<NS>(v.w, T, U, cs, cu);
+    auto addr = [&](int64_t id) -> const uint16_t* {
+        return (ld == cols) ? x + id * 8 : x + (id / cpr) * ld + (id % cpr) * 8;
+    };
+    auto count8 = [&](const uint4& v) {
+        count2<NS>(v.x, T2, U2, ps, pu, pz);
+        count2<NS>(v.y, T2, U2, ps, pu, pz);
+        count2<NS>(v.z, T2, U2, ps, pu, pz);
+        count2<NS>(v.w, T2, U2, ps, pu, pz);
+    };
+    int steps = 0;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + tid;
+    for (; i + 3 * stride < total; i += 4 * stride) {  // four loads in flight per thread
+        const uint4 v0 = ld_stream_v4(addr(i)), v1 = ld_stream_v4(addr(i + stride));
+        const uint4 v2 = ld_stream_v4(addr(i + 2 * stride)), v3 = ld_stream_v4(addr(i + 3 * stride));
+        count8(v0);
+        count8(v1);
+        count8(v2);
+        count8(v3);
+        if (++steps == 2048) {
+            fold();
+            steps = 0;
+        }
     }
+    for (; i < total; i += stride) count8(ld_stream_v4(addr(i)));  // fewer than four steps: no fold needed
+    fold();
+#pragma unroll
+    for (int j = 0; j < NS; ++j) cu[j] -= cz;  // |x| <= U_j counted the zeros too
 #pragma unroll
     for (int j = 0; j < NS; ++j) {
         cs[j] = __reduce_add_sync(0xffffffffu, cs[j]);
@@ -147,12 +207,16 @@ __global__ void __launch_bounds__(kStatsThreads)
 template <int FMT, int NS>
 fp8_status launch_stats(const void* x, int64_t rows, int64_t cols, int64_t ld, const float* scales, int n,
                         uint64_t* saturated, uint64_t* underflow, cudaStream_t st) {
+    auto k = cast_stats_kernel<FMT, NS>;
+    int occ = 0;  // grid-stride CTAs: no more than fit at once (the thresholds are found once per CTA)
+    fp8_status s = resident_ctas(reinterpret_cast<const void*>(k), kStatsThreads, 0, &occ);
+    if (s != FP8_OK) return s;
     const int64_t chunks = rows * (cols / 8);
     int64_t grid = (chunks + kStatsThreads - 1) / kStatsThreads;
-    const int64_t cap = (int64_t)device_sm_count() * 8;
+    const int64_t cap = (int64_t)device_sm_count() * occ;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    cast_stats_kernel<FMT, NS><<<(int)grid, kStatsThreads, 0, st>>>(
+    k<<<(int)grid, kStatsThreads, 0, st>>>(
         static_cast<const uint16_t*>(x), rows, cols, ld, scales, n, reinterpret_cast<unsigned long long*>(saturated),
         reinterpret_cast<unsigned long long*>(underflow));
     return check_launch("cast_stats kernel launch");
