@@ -204,9 +204,12 @@ __device__ __forceinline__ void stage_col32(uint32_t base, int c, int seg, const
 // rows t/16 + 16 i, i = 0..7.  Column pass: warp w covers column pairs
 // lane + 32 (w & 1) over the 32-row segment w / 2.
 // The tile loop (shared by the cast kernel and the fused current-scaling kernel).  For
-// per-tensor scaling `s_given` is the scale; block granularities compute their own.
+// per-tensor scaling `s_given` is the scale; block granularities compute their own.  With
+// `from_end` the CTAs walk the tiles from the last one back (the fused kernel's amax pass reads x
+// front to back, so the tiles it read last are the likeliest to be still in L2).
 template <int GRAN, int FMT>
-__device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const QuantArgs& a, float s_given) {
+__device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const QuantArgs& a, float s_given,
+                                               bool from_end = false) {
     const CUtensorMap* tmX = &maps->x;
     extern __shared__ uint8_t smem_raw[];
     QuantSmem& S = *reinterpret_cast<QuantSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -232,7 +235,7 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
     // slower with the hint and load without it.
     const uint64_t policy = GRAN == FP8_SCALE_TENSOR && tid == 0 ? l2_policy_evict_first() : 0;
     auto issue = [&](int64_t i) {  // TMA load of this CTA's i-th tile into stage i % kQStages
-        const int64_t tile = blockIdx.x + i * gridDim.x;
+        const int64_t tile = from_end ? a.ntiles - 1 - (blockIdx.x + i * gridDim.x) : blockIdx.x + i * gridDim.x;
         const int st = (int)(i % kQStages);
         const int x0 = (int)((tile % a.tiles_c) * kTile), y0 = (int)((tile / a.tiles_c) * kTile);
         mbar_arrive_expect_tx(smem_u32(&S.full[st]), kTile * kTile * 2);
@@ -280,7 +283,7 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
             break;
         }
         const uint16_t* T = S.tile[st];
-        const int64_t tile = blockIdx.x + i * gridDim.x;
+        const int64_t tile = from_end ? a.ntiles - 1 - (blockIdx.x + i * gridDim.x) : blockIdx.x + i * gridDim.x;
         const int64_t r0 = (tile / a.tiles_c) * kTile, c0 = (tile % a.tiles_c) * kTile;
         const int64_t col = c0 + 8 * j;
         const bool col_ok = col < a.cols;
@@ -571,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (s_abort) return;
 
     // phase 2: the cast
-    quantize_tiles<FP8_SCALE_TENSOR, FMT>(&maps, a, s_scale);
+    quantize_tiles<FP8_SCALE_TENSOR, FMT>(&maps, a, s_scale, /*from_end=*/true);
 }
 
 // Per-tensor scaled cast of an fp32 tensor: q = Encode(fl32(x s)), grid-stride over 8-element
