@@ -221,8 +221,9 @@ FP8Q_API fp8_status fp8_cast_stats(const void *x, int64_t rows, int64_t cols, in
  *              exceeds 1.75.  Not the default; scales stored as for MX.
  *              A partial block at an edge uses the elements that exist.
  *   margin   used by the block granularities only.
- *   q_row    device u8 [rows x cols] (dense), or NULL.
- *   q_col    device u8 [cols x rows] (dense, the transposed copy), or NULL.
+ *   q_row    device u8 [rows x cols] (dense, 8-byte aligned), or NULL.
+ *   q_col    device u8 [cols x rows] (dense, the transposed copy, 16-byte
+ *            aligned), or NULL.  Misalignment of either is UNSUPPORTED.
  *            At least one of q_row / q_col.  With q_col, rows must be a
  *            multiple of 16.  The column-wise copy is the row-wise
  *            quantisation of x transposed: per-tensor and 128x128 use the same
