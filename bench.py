@@ -231,7 +231,11 @@ def run_ours(args, rank, world):
         "roofline": {"bound": "tensor", "kernel": "gemm_tensor_pair_kernel (13B FFN fprop/dgrad/wgrad)",
                      "achieved": round(tensor_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(tensor_tflops / fp8_peak, 4), "peak_source": peak_note,
-                     "traffic": traffic},
+                     "traffic": traffic,
+                     # context: the step runs under the power cap, where the measured sustained bf16
+                     # figure (a seconds-long cuBLAS loop) is the like-for-like denominator
+                     "frac_of_sustained": round(
+                         tensor_tflops / (pk["bf16_tflops_sustained"] * FP8_OVER_BF16), 4)},
         "roofline_quantizer": {"bound": "hbm", "kernel": "quantize_tile_kernel (all casts of the step)",
                                "achieved": round(quant_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                                "frac": round(quant_gbs / pk["hbm_gbs"], 4), "peak_source": pk_src,
