@@ -24,6 +24,7 @@ For N > 1 launch with torchrun; every rank runs an independent replica.
 from __future__ import annotations
 
 import argparse
+import math
 import json
 import os
 import statistics
@@ -40,6 +41,7 @@ METRIC = "quantize GB/s and FP8 scaled-GEMM TFLOPS at 1 GB300, % of HBM/FP8 roof
 WORKLOAD = ("fp8 training hot path step: per-tensor current-scaling fwd 256x1024x1024 + 13B FFN fwd+bwd "
             "16384x20480x5120 per-tensor delayed (L=1024, row+col casts) + MXFP8 fwd 16384x28672x8192 "
             "(row+col casts) + per-block 1x128/128x128 fwd 8192x11008x4096")
+REFERENCE_BUDGET_S = 120.0  # wall time the reference arm aims for, warm-up and timed steps together
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio 4.5 / 2.25 PFLOP/s
 
@@ -493,8 +495,15 @@ def run_reference(args, rank, world):
     import oracle as o
     o.lib()
     host = make_inputs()
-    R = args.reference_rows
     ffn = ffn_scales(host)
+    R = args.reference_rows
+    if R <= 0:
+        # size the sample so that the warm-up and timed steps take about two minutes together: the
+        # oracle's work per step grows about as R^2 (an R x R output block of each GEMM)
+        f0, t0 = oracle_step_sample(host, 64, ffn)
+        per_step = REFERENCE_BUDGET_S / (args.warmup + args.steps)
+        R = int(64 * math.sqrt(per_step / max(t0, 1e-6)))
+        R = max(16, min(512, R - R % 16))
     for _ in range(args.warmup):
         oracle_step_sample(host, R, ffn)
     tot_f, tot_s = 0.0, 0.0
@@ -625,7 +634,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--reference-rows", type=int, default=128)
+    ap.add_argument("--reference-rows", type=int, default=0,
+                    help="rows of each GEMM's operands the reference arm samples (0: sized to the step count)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true", help="skip the rows measured beside the step")
     ap.add_argument("--case", choices=sorted(PROFILE_CASES), default=None,
