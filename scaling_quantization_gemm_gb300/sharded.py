@@ -30,9 +30,14 @@ from .step import LinearFwdBwd
 
 
 def allreduce_amax_(amax: torch.Tensor, group: Optional[dist.ProcessGroup] = None) -> torch.Tensor:
-    """In place: amax <- max over ranks (fp32; NaN propagates like a local amax)."""
+    """In place: amax <- max over ranks (fp32).
+
+    An amax is |x| of some element: a non-negative float, +Inf or a NaN with the sign bit clear, whose
+    bit patterns, read as int32, order exactly as the values do, with every NaN above +Inf.  The
+    reduction is a MAX over those integers, so a NaN on any rank reaches every rank (a floating-point
+    MAX keeps or drops a NaN depending on the order of its operands)."""
     if dist.is_initialized() and dist.get_world_size(group) > 1:
-        dist.all_reduce(amax, op=dist.ReduceOp.MAX, group=group)
+        dist.all_reduce(amax.view(torch.int32), op=dist.ReduceOp.MAX, group=group)
     return amax
 
 

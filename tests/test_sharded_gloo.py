@@ -25,6 +25,16 @@ def _worker(rank, world, port, q):
 
     a = torch.tensor([1.5 if rank == 0 else 7.25])
     allreduce_amax_(a)
+    # a non-finite amax on one rank reaches both, whichever rank holds it
+    specials = []
+    for bad_rank in (0, 1):
+        for bad in (float("nan"), float("inf")):
+            v = torch.tensor([bad if rank == bad_rank else 3.0])
+            allreduce_amax_(v)
+            specials.append(v.item())
+    z = torch.tensor([0.0])
+    allreduce_amax_(z)
+    specials.append(z.item())
     s = torch.arange(6, dtype=torch.float32) * (rank + 1)
     allreduce_sum_(s)
 
@@ -36,7 +46,8 @@ def _worker(rank, world, port, q):
         local = torch.tensor([float(oracle.amax(shard))])
         allreduce_amax_(local)
         hist.update(float(local[0]), 1, 1)
-    q.put((rank, float(a[0]), s.tolist(), hist.hist.tolist(), int(hist.bias[0]), float(hist.scale[0])))
+    q.put((rank, float(a[0]), s.tolist(), hist.hist.tolist(), int(hist.bias[0]), float(hist.scale[0]),
+           [repr(v) for v in specials]))
     dist.destroy_process_group()
 
 
@@ -53,8 +64,9 @@ def test_sharded_reductions_and_delayed_scaling_gloo():
         assert p.exitcode == 0
     res = dict((r[0], r[1:]) for r in (q.get(timeout=10) for _ in range(world)))
     assert res[0] == res[1]  # identical scaling state on every rank
-    amax, s, hist, bias, scale = res[0]
+    amax, s, hist, bias, scale, specials = res[0]
     assert amax == 7.25
+    assert specials == ["nan", "inf", "nan", "inf", "0.0"]
     assert s == [3.0 * i for i in range(6)]
     # the unsharded reference: the same six tensors, whole
     import oracle
