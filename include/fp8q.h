@@ -209,7 +209,8 @@ FP8Q_API fp8_status fp8_cast_stats(const void *x, int64_t rows, int64_t cols, in
  *   q = RNE_saturate_fmt(x * 2^e) with the product taken in fp32.
  *
  *   x        device, bf16 [rows x cols], leading dimension ld; 16-byte aligned,
- *            cols and ld multiples of 8.
+ *            cols and ld multiples of 8; rows and cols below 2^31 (else
+ *            UNSUPPORTED: tiles are addressed with 32-bit coordinates).
  *   gran     FP8_SCALE_TENSOR: e from `scale` (device fp32 2^e, required);
  *              sf_row and sf_col must be NULL.
  *            FP8_SCALE_BLOCK_1x128 / _128x128 / FP8_SCALE_MX_1x32: each block

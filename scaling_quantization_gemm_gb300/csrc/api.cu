@@ -61,6 +61,13 @@ fp8_status check_bf16_matrix(const void* x, int64_t rows, int64_t cols, int64_t 
     return FP8_OK;
 }
 
+// The casts address x and the column-wise output through TMA tensor maps, whose coordinates are 32-bit.
+fp8_status check_tma_dims(int64_t rows, int64_t cols) {
+    FP8_REQUIRE(rows < (1ll << 31) && cols < (1ll << 31), FP8_ERR_UNSUPPORTED,
+                "rows and cols must be below 2^31 (rows=%lld cols=%lld)", (long long)rows, (long long)cols);
+    return FP8_OK;
+}
+
 }  // namespace
 }  // namespace fp8q
 
@@ -127,6 +134,8 @@ fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, f
     g_detail[0] = 0;
     fp8_status s = check_bf16_matrix(x, rows, cols, ld);
     if (s != FP8_OK) return s;
+    s = check_tma_dims(rows, cols);
+    if (s != FP8_OK) return s;
     FP8_REQUIRE(valid_fmt(fmt), FP8_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
     FP8_REQUIRE(valid_gran(gran), FP8_ERR_INVALID_ARG, "unknown granularity %d", (int)gran);
     if (rows == 0 || cols == 0) return FP8_OK;
@@ -161,6 +170,8 @@ fp8_status fp8_quantize_current(const void* x, int64_t rows, int64_t cols, int64
     g_detail[0] = 0;
     fp8_status s = check_bf16_matrix(x, rows, cols, ld);
     if (s != FP8_OK) return s;
+    s = check_tma_dims(rows, cols);
+    if (s != FP8_OK) return s;
     FP8_REQUIRE(valid_fmt(fmt), FP8_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
     FP8_REQUIRE(workspace != nullptr, FP8_ERR_INVALID_ARG, "workspace is NULL");
     FP8_REQUIRE(aligned(workspace, 16), FP8_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
@@ -185,6 +196,8 @@ fp8_status fp8_quantize_current_noalloc(const void* x, int64_t rows, int64_t col
                                         float* scale, float* scale_inv, int32_t* status, void* stream) {
     g_detail[0] = 0;
     fp8_status s = check_bf16_matrix(x, rows, cols, ld);
+    if (s != FP8_OK) return s;
+    s = check_tma_dims(rows, cols);
     if (s != FP8_OK) return s;
     FP8_REQUIRE(valid_fmt(fmt), FP8_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
     FP8_REQUIRE((!amax || aligned(amax, 4)) && (!bias || aligned(bias, 4)) && (!scale || aligned(scale, 4)) &&

@@ -198,3 +198,13 @@ def test_quantize_f32_validation(L):
     assert f(FAKE + 4, 8, 0, None, FAKE, None, None) == 2      # x not 16-byte aligned
     assert f(FAKE, 8, 0, None, FAKE + 2, None, None) == 2      # q not 8-byte aligned
     assert f(FAKE, 8, 0, FAKE + 1, FAKE, None, None) == 1      # scale misaligned
+
+
+def test_cast_dimensions_past_2_31_rejected(L):
+    big = 1 << 31
+    # fp8_quantize / fp8_quantize_current / _noalloc: TMA coordinates are 32-bit
+    assert L.fp8_quantize(FAKE, big, 8, 8, 0, 0, 0, FAKE, FAKE, None, None, None, None, None) == 2
+    assert L.fp8_quantize(FAKE, 8, big, big, 0, 0, 0, FAKE, FAKE, None, None, None, None, None) == 2
+    assert L.fp8_quantize_current(FAKE, big, 8, 8, 0, 0, FAKE, None, None, None, None, None, FAKE, None, None) == 2
+    assert L.fp8_quantize_current_noalloc(FAKE, 8, big, big, 0, 0, FAKE, None, None, None, None, None, None,
+                                          None) == 2
