@@ -162,6 +162,38 @@ FP8Q_API fp8_status fp8_amax_history_update(float *history, int32_t len, int64_t
                                    int32_t *status, void *stream);
 
 /*
+ * fp8_amax_history_update_batch -- fp8_amax_history_update for n independent
+ * delayed-scaling states in one launch.
+ * Source: as fp8_amax_history_update (delayed scaling, "Per-Tensor and
+ * Per-Block Scaling Strategies for Effective FP8 Training", "Key Questions
+ * Answered").  A model keeps one state per FP8 tensor; updating them together
+ * takes one kernel launch per 48 states instead of one per state.
+ *
+ *   states   HOST array of n records, read during the call only.  Each record
+ *            holds the arguments of one fp8_amax_history_update call: device
+ *            pointers history, pos, amax, bias, scale and scale_inv (all
+ *            required) and status (or NULL); len in [1, 65536]; fmt; margin.
+ *            `reserved` must be 0.  Records must not share history, pos,
+ *            amax, bias, scale or scale_inv (they may share a status word).
+ *   n        number of records, n >= 0; 0 is a no-op (states may then be NULL).
+ * Every state ends exactly as fp8_amax_history_update would leave it.
+ */
+typedef struct {
+    float *history;
+    int64_t *pos;
+    float *amax;
+    int32_t *bias;
+    float *scale;
+    float *scale_inv;
+    int32_t *status;
+    int32_t len;
+    int32_t fmt;    /* fp8_format */
+    int32_t margin;
+    int32_t reserved;
+} fp8_history_state;
+FP8Q_API fp8_status fp8_amax_history_update_batch(const fp8_history_state *states, int32_t n, void *stream);
+
+/*
  * fp8_set_bias -- a fixed exponent bias (FP8-CSCALE).
  * Source: fixed scaling, a bias chosen once per tensor instead of derived
  * from its amax, compared against FP8-AMAX in a sweep of fixed values

@@ -33,6 +33,7 @@ STATUS_NONFINITE_AMAX, STATUS_TIMEOUT, STATUS_BAD_BLOCK_SCALE = 1, 2, 4
 
 # every entry point declared in include/fp8q.h
 ENTRY_POINTS = ("fp8_amax", "fp8_compute_scale", "fp8_compute_scale_ratio", "fp8_amax_history_update",
+                "fp8_amax_history_update_batch",
                 "fp8_set_bias", "fp8_cast_stats", "fp8_quantize", "fp8_quantize_f32", "fp8_quantize_current",
                 "fp8_quantize_current_noalloc",
                 "fp8_scaled_gemm", "fp8_scaled_gemm_quantize", "fp8_status_string", "fp8_last_error_detail")
@@ -64,6 +65,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_compute_scale": [vp, i32, i32, vp, vp, vp, vp, vp],
                 "fp8_compute_scale_ratio": [vp, i32, vp, vp, vp, vp],
                 "fp8_amax_history_update": [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp],
+                "fp8_amax_history_update_batch": [vp, i32, vp],
                 "fp8_quantize": [vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp],
                 "fp8_quantize_f32": [vp, i64, i32, vp, vp, vp, vp],
                 "fp8_set_bias": [i32, vp, vp, vp, vp],
@@ -146,6 +148,28 @@ def fp8_amax_history_update(history: torch.Tensor, pos: Ptr, amax: Ptr, fmt: int
     _check("fp8_amax_history_update",
            lib().fp8_amax_history_update(_p(history), history.numel(), _p(pos), _p(amax), fmt, margin, _p(bias),
                                          _p(scale), _p(scale_inv), _p(status), _stream(stream)))
+
+
+class HistoryStateRecord(ctypes.Structure):
+    """One record of fp8_amax_history_update_batch (fp8_history_state in fp8q.h)."""
+    _fields_ = [("history", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("amax", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("scale_inv", ctypes.c_void_p),
+                ("status", ctypes.c_void_p), ("len", ctypes.c_int32), ("fmt", ctypes.c_int32),
+                ("margin", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+def fp8_amax_history_update_batch(states, stream=None) -> None:
+    """fp8_amax_history_update for every state in `states` in one launch per 48.  Each state is an object
+    with tensors history, pos, amax, bias, scale, scale_inv (and optionally status) and ints fmt, margin."""
+    states = list(states)
+    recs = (HistoryStateRecord * max(len(states), 1))()
+    for r, st in zip(recs, states):
+        r.history, r.pos, r.amax = _p(st.history), _p(st.pos), _p(st.amax)
+        r.bias, r.scale, r.scale_inv = _p(st.bias), _p(st.scale), _p(st.scale_inv)
+        r.status = _p(getattr(st, "status", None))
+        r.len, r.fmt, r.margin, r.reserved = st.history.numel(), int(st.fmt), int(st.margin), 0
+    _check("fp8_amax_history_update_batch",
+           lib().fp8_amax_history_update_batch(ctypes.cast(recs, ctypes.c_void_p), len(states), _stream(stream)))
 
 
 def fp8_set_bias(e: int, bias: Ptr = None, scale: Ptr = None, scale_inv: Ptr = None, stream=None) -> None:
@@ -234,7 +258,7 @@ def fp8_scaled_gemm_quantize(op: int, A: torch.Tensor, fa: int, sfa: Ptr, B: tor
 
 
 __all__ = ["lib", "FP8Error", "status_name", "fp8_amax", "fp8_compute_scale", "fp8_compute_scale_ratio",
-           "fp8_amax_history_update",
+           "fp8_amax_history_update", "fp8_amax_history_update_batch", "HistoryStateRecord",
            "fp8_set_bias", "fp8_cast_stats",
            "fp8_quantize", "fp8_quantize_f32", "fp8_quantize_current", "fp8_quantize_current_noalloc",
            "current_workspace", "fp8_scaled_gemm", "fp8_scaled_gemm_quantize", "ENTRY_POINTS",

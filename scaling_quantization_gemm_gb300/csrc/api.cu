@@ -32,6 +32,7 @@ fp8_status launch_quantize_current_noalloc(const void* x, int64_t rows, int64_t 
                                            int margin, uint8_t* q_row, uint8_t* q_col, float* amax, int32_t* bias,
                                            float* scale, float* scale_inv, int32_t* status, cudaStream_t st);
 fp8_status launch_set_bias(int e, int32_t* bias, float* scale, float* scale_inv, cudaStream_t st);
+fp8_status launch_history_batch(const fp8_history_state* states, int n, cudaStream_t st);
 fp8_status launch_quantize_f32(const float* x, int64_t n, int fmt, const float* scale, uint8_t* q, float* amax,
                                cudaStream_t st);
 fp8_status launch_cast_stats(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, const float* scales,
@@ -126,6 +127,28 @@ fp8_status fp8_amax_history_update(float* history, int32_t len, int64_t* pos, fl
     FP8_REQUIRE(valid_fmt(fmt), FP8_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
     FP8_REQUIRE(aligned(pos, 8), FP8_ERR_INVALID_ARG, "pos must be 8-byte aligned");
     return launch_history(history, len, pos, amax, fmt, margin, bias, scale, scale_inv, status, as_stream(stream));
+}
+
+static_assert(sizeof(fp8_history_state) == 72, "fp8_history_state is part of the ABI: 7 pointers and 4 int32");
+
+fp8_status fp8_amax_history_update_batch(const fp8_history_state* states, int32_t n, void* stream) {
+    g_detail[0] = 0;
+    FP8_REQUIRE(n >= 0, FP8_ERR_INVALID_ARG, "negative count %d", (int)n);
+    if (n == 0) return FP8_OK;
+    FP8_REQUIRE(states != nullptr, FP8_ERR_INVALID_ARG, "states is NULL");
+    for (int32_t i = 0; i < n; ++i) {
+        const fp8_history_state& t = states[i];
+        FP8_REQUIRE(t.history && t.pos && t.amax && t.bias && t.scale && t.scale_inv, FP8_ERR_INVALID_ARG,
+                    "record %d: history, pos, amax, bias, scale and scale_inv are required", (int)i);
+        FP8_REQUIRE(t.len >= 1 && t.len <= 65536, FP8_ERR_INVALID_ARG, "record %d: len must be in [1, 65536] (got %d)",
+                    (int)i, (int)t.len);
+        FP8_REQUIRE(valid_fmt(t.fmt), FP8_ERR_INVALID_ARG, "record %d: unknown format %d", (int)i, (int)t.fmt);
+        FP8_REQUIRE(t.reserved == 0, FP8_ERR_INVALID_ARG, "record %d: reserved must be 0", (int)i);
+        FP8_REQUIRE(aligned(t.pos, 8) && aligned(t.history, 4) && aligned(t.amax, 4) && aligned(t.bias, 4) &&
+                        aligned(t.scale, 4) && aligned(t.scale_inv, 4) && (!t.status || aligned(t.status, 4)),
+                    FP8_ERR_INVALID_ARG, "record %d: misaligned pointer (pos 8 bytes, the others 4)", (int)i);
+    }
+    return launch_history_batch(states, n, as_stream(stream));
 }
 
 fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, fp8_format fmt, fp8_granularity gran,

@@ -664,9 +664,8 @@ __global__ void compute_scale_ratio_kernel(const float* amax, int fmt, float* sc
 }
 
 // One delayed-scaling step in one CTA: record, window max, bias, reset.
-__global__ void __launch_bounds__(1024) history_kernel(float* hist, int len, int64_t* pos, float* amax, int fmt,
-                                                       int margin, int32_t* bias, float* scale, float* scale_inv,
-                                                       int32_t* status) {
+__device__ __forceinline__ void history_step(float* hist, int len, int64_t* pos, float* amax, int fmt, int margin,
+                                             int32_t* bias, float* scale, float* scale_inv, int32_t* status) {
     __shared__ int64_t p_s;
     __shared__ uint32_t red[32];
     if (threadIdx.x == 0) {
@@ -693,6 +692,23 @@ __global__ void __launch_bounds__(1024) history_kernel(float* hist, int len, int
         *pos = p_s + 1;
         if (nf && status) atomicOr(status, FP8_STATUS_NONFINITE_AMAX);
     }
+}
+
+__global__ void __launch_bounds__(1024) history_kernel(float* hist, int len, int64_t* pos, float* amax, int fmt,
+                                                       int margin, int32_t* bias, float* scale, float* scale_inv,
+                                                       int32_t* status) {
+    history_step(hist, len, pos, amax, fmt, margin, bias, scale, scale_inv, status);
+}
+
+// Many independent delayed-scaling states in one launch: CTA b runs the step of state b.
+constexpr int kHistBatch = 48;  // records per launch (48 x 72 bytes of kernel parameters)
+struct HistBatch {
+    fp8_history_state s[kHistBatch];
+};
+
+__global__ void __launch_bounds__(1024) history_batch_kernel(const __grid_constant__ HistBatch b) {
+    const fp8_history_state& st = b.s[blockIdx.x];
+    history_step(st.history, st.len, st.pos, st.amax, st.fmt, st.margin, st.bias, st.scale, st.scale_inv, st.status);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 q_encode_fn() {
@@ -812,6 +828,24 @@ fp8_status launch_history(float* hist, int len, int64_t* pos, float* amax, int f
     const int threads = len >= 1024 ? 1024 : ((len + 31) / 32) * 32;
     history_kernel<<<1, threads, 0, st>>>(hist, len, pos, amax, fmt, margin, bias, scale, scale_inv, status);
     return check_launch("history kernel launch");
+}
+
+fp8_status launch_history_batch(const fp8_history_state* states, int n, cudaStream_t st) {
+    for (int first = 0; first < n; first += kHistBatch) {
+        const int cnt = n - first < kHistBatch ? n - first : kHistBatch;
+        HistBatch b;
+        memset(&b, 0, sizeof(b));
+        int longest = 1;
+        for (int i = 0; i < cnt; ++i) {
+            b.s[i] = states[first + i];
+            longest = b.s[i].len > longest ? b.s[i].len : longest;
+        }
+        const int threads = longest >= 1024 ? 1024 : ((longest + 31) / 32) * 32;
+        history_batch_kernel<<<cnt, threads, 0, st>>>(b);
+        fp8_status s = check_launch("history batch kernel launch");
+        if (s != FP8_OK) return s;
+    }
+    return FP8_OK;
 }
 
 namespace {

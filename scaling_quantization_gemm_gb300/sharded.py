@@ -25,7 +25,7 @@ from typing import Optional
 import torch
 import torch.distributed as dist
 
-from . import E4M3, E5M2, TENSOR, fp8_amax, fp8_compute_scale, fp8_quantize
+from . import E4M3, E5M2, TENSOR, fp8_amax, fp8_amax_history_update_batch, fp8_compute_scale, fp8_quantize
 from .step import LinearFwdBwd
 
 
@@ -77,10 +77,13 @@ class ShardedLinearFwdBwd(LinearFwdBwd):
 
     def advance(self) -> None:
         # the first step's amax is already the reduced one; later steps reduce the fused local amax
-        for st in (self.sx, self.sw, self.sg):
+        states = (self.sx, self.sw, self.sg)
+        for st in states:
             if st.steps > 0:
                 allreduce_amax_(st.amax, self.group)
-            st.advance()
+        fp8_amax_history_update_batch(states)
+        for st in states:
+            st.steps += 1
 
 
 __all__ = ["allreduce_amax_", "allreduce_sum_", "ShardedLinearFwdBwd", "E4M3", "E5M2"]

@@ -37,7 +37,8 @@ from typing import Optional
 import torch
 
 from . import (BLOCK_1x128, BLOCK_128x128, DGRAD, E4M3, E5M2, FPROP, MX_1x32, MX_1x32_OCP, TENSOR, WGRAD,
-               current_workspace, fp8_amax, fp8_amax_history_update, fp8_cast_stats, fp8_compute_scale,
+               current_workspace, fp8_amax, fp8_amax_history_update, fp8_amax_history_update_batch, fp8_cast_stats,
+               fp8_compute_scale,
                fp8_compute_scale_ratio, fp8_quantize, fp8_quantize_current, fp8_scaled_gemm, fp8_scaled_gemm_quantize,
                fp8_set_bias)
 
@@ -188,8 +189,11 @@ class LinearFwdBwd:
                         self.sx.scale_inv, self.dW)
 
     def advance(self) -> None:
-        for st in (self.sx, self.sw, self.sg):
-            st.advance()
+        """The three delayed-scaling updates in one launch."""
+        states = (self.sx, self.sw, self.sg)
+        fp8_amax_history_update_batch(states)
+        for st in states:
+            st.steps += 1
 
     def run(self) -> None:
         self.quantize()

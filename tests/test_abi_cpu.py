@@ -208,3 +208,23 @@ def test_cast_dimensions_past_2_31_rejected(L):
     assert L.fp8_quantize_current(FAKE, big, 8, 8, 0, 0, FAKE, None, None, None, None, None, FAKE, None, None) == 2
     assert L.fp8_quantize_current_noalloc(FAKE, 8, big, big, 0, 0, FAKE, None, None, None, None, None, None,
                                           None) == 2
+
+
+def test_history_batch_validation(L):
+    import scaling_quantization_gemm_gb300 as q
+    assert ctypes.sizeof(q.HistoryStateRecord) == 72  # fp8_history_state
+    f = L.fp8_amax_history_update_batch
+    assert f(None, 0, None) == 0  # empty: no-op
+    assert f(None, -1, None) == 1
+    assert f(None, 2, None) == 1
+    recs = (q.HistoryStateRecord * 2)()
+    for r in recs:
+        r.history = r.pos = r.amax = r.bias = r.scale = r.scale_inv = FAKE
+        r.len, r.fmt = 16, 0
+    addr = ctypes.cast(recs, ctypes.c_void_p)
+    # record 1 invalid in turn: rejected before any launch
+    for field, bad, good in (("len", 0, 16), ("len", 65537, 16), ("fmt", 7, 1), ("reserved", 3, 0),
+                             ("pos", FAKE + 4, FAKE), ("status", FAKE + 2, None), ("scale", None, FAKE)):
+        setattr(recs[1], field, bad)
+        assert f(addr, 2, None) == 1, field
+        setattr(recs[1], field, good)
