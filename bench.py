@@ -122,6 +122,18 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power)}
 
 
+def clock_suspect(summary) -> list:
+    """Why a timed region's clock record makes its number invalid (empty if it is valid): hardware or
+    thermal slowdown, or an SM clock far below its maximum with no reason reported (a clock lock left
+    behind by another user).  The software power cap is normal under load and kept."""
+    reasons = set(summary.get("reasons") or [])
+    bad = sorted(reasons & {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"})
+    sm, sm_max = summary.get("sm_mhz"), summary.get("sm_max_mhz")
+    if sm and sm_max and not reasons and sm < 0.75 * sm_max:
+        bad.append("sm_clock_low_without_reason")
+    return bad
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -204,13 +216,7 @@ def run_ours(args, rank, world):
         return total, ops_ms, sampler.summary()
 
     total_ms, per_op, clock_summary = timed()
-    # a timed region that saw hardware or thermal slowdown, or an SM clock far below its maximum with no
-    # reason reported (a clock lock left by someone else), is not a valid number: time it once more
-    suspect = sorted(set(clock_summary.get("reasons", [])) & {"hw_slowdown", "hw_thermal_slowdown",
-                                                              "sw_thermal_slowdown"})
-    if (clock_summary.get("sm_mhz") and not clock_summary["reasons"]
-            and clock_summary["sm_mhz"] < 0.75 * clock_summary["sm_max_mhz"]):
-        suspect.append("sm_clock_low_without_reason")
+    suspect = clock_suspect(clock_summary)
     if max_over_ranks(1.0 if suspect else 0.0, world) > 0:
         total_ms, per_op, clock_summary = timed()
         clock_summary["remeasured_after"] = suspect or ["another rank"]
