@@ -242,7 +242,7 @@ def run_ours(args, rank, world):
 
     nxt = measure_next_rows(args, dev, c5, pk, stream) if not args.no_next_rows else None
 
-    cpu = cpu_baseline(host) if (rank == 0 and not args.no_cpu_baseline) else None
+    cpu = cpu_baseline(host, step_flops) if (rank == 0 and not args.no_cpu_baseline) else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
@@ -499,14 +499,31 @@ def oracle_step_sample(host, R: int, ffn):
     return flops, time.time() - t0
 
 
-def cpu_baseline(host, R: int = 512):
+def cpu_baseline(host, step_flops: float, R: int = 512):
     import oracle as o
     o.lib()
     flops, sec = oracle_step_sample(host, R, ffn_scales(host))
-    return {"value": round(flops / sec / 1e12, 6), "unit": "TFLOP/s", "cores": o.max_threads(), "kind": "oracle",
+    cores = o.max_threads()
+    # the oracle's casts (per-tensor and MX, row + column-wise) on one thread and on all cores, over
+    # 1024 rows of the FFN gradient (21 M elements); GB/s of algorithmic bytes as for the GPU casts
+    xs = np.ascontiguousarray(host["dY5"][:1024])
+    scale = o.scale_triple(o.amax(xs), 1, 1)[1]
+    cast_rates = {}
+    for nthreads in (1, cores):
+        o.set_threads(nthreads)
+        t0 = time.time()
+        o.quantize_tensor(xs, 1, scale, row=True, col=True)
+        o.quantize_block(xs, 1, o.MX_1x32, 0, row=True, col=True)
+        cast_rates[nthreads] = (4.0 + 4.0 + 2.0 / 32) * xs.size / (time.time() - t0) / 1e9
+    o.set_threads(cores)
+    value = flops / sec
+    return {"value": round(value / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{R}x{R} output block of each of the 6 GEMMs of the step, its operand rows cast by the "
                       f"oracle (current scaling from whole-tensor amax, the FFN layer from its delayed-scaling "
-                      f"history); {flops / 1e9:.2f} GFLOP in {sec:.1f} s"}
+                      f"history); {flops / 1e9:.2f} GFLOP in {sec:.1f} s",
+            "extrapolated_full_step_s": round(step_flops / value, 1),
+            "cast_gbs_1_thread": round(cast_rates[1], 3), "cast_gbs_all_cores": round(cast_rates[cores], 3),
+            "cast_sample": "per-tensor and MX casts, row + column-wise, of 1024 x 20480 bf16 (the FFN gradient)"}
 
 
 def run_reference(args, rank, world):
