@@ -127,6 +127,35 @@ def test_gemm_exact_block(oracle, ga, gb):
         assert abs(Fraction(y[i]) - ref[m][n]) <= abs(ref[m][n]) * Fraction(1, 2 ** 50)
 
 
+@pytest.mark.parametrize("ga,gb", [(3, 3), (1, 2), (1, 1)])
+def test_gemm_full_exact_block(oracle, ga, gb):
+    """The whole product with distinct block scales per row and per K block, element by element
+    against exact rational arithmetic (rows and K blocks both cross the scale-block edges)."""
+    rng = np.random.default_rng(30 + ga + 10 * gb)
+    M, N, K = 5, 133, 256
+    A = _finite_codes(rng, (M, K), 0)
+    B = _finite_codes(rng, (N, K), 1)
+    if ga == 3:
+        sfa = rng.integers(118, 137, (M, K // 32)).astype(np.uint8)
+        sfb = rng.integers(118, 137, (N, K // 32)).astype(np.uint8)
+        fa_ = lambda m, k: Fraction(2) ** (int(sfa[m, k // 32]) - 127)
+        fb_ = lambda n, k: Fraction(2) ** (int(sfb[n, k // 32]) - 127)
+    else:
+        sfa = np.ldexp(np.float32(1), rng.integers(-6, 7, (M, K // 128))).astype(np.float32)
+        rb = N if gb == 1 else -(-N // 128)
+        sfb = np.ldexp(np.float32(1), rng.integers(-6, 7, (rb, K // 128))).astype(np.float32)
+        fa_ = lambda m, k: Fraction(float(sfa[m, k // 128]))
+        fb_ = (lambda n, k: Fraction(float(sfb[n, k // 128]))) if gb == 1 else \
+              (lambda n, k: Fraction(float(sfb[n // 128, k // 128])))
+    y, mag = oracle.gemm_full(A, 0, ga, sfa, B, 1, gb, sfb)
+    ref = _exact_gemm(A, 0, fa_, B, 1, fb_, oracle)
+    for m in range(M):
+        for n in range(N):
+            # fp64 summation of K products with cancellation: within K ulps of sum |a b|
+            assert abs(Fraction(y[m, n]) - ref[m][n]) <= Fraction(float(mag[m, n])) * K * Fraction(1, 2 ** 52), (m, n)
+    assert np.all(mag >= np.abs(y))
+
+
 def test_gemm_identity_weight(oracle):
     """B = 2^j I: y = deq(A) 2^j exactly."""
     rng = np.random.default_rng(0)

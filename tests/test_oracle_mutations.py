@@ -1,0 +1,78 @@
+"""Planted mistakes in the oracle: each case compiles a copy of the oracle's C source with one
+plausible mistake (a wrong tie rule, an off-by-one exponent, a flipped margin sign, a window that
+forgets its history, a scale read from the wrong row, a column-wise copy in the wrong order, a
+subnormal decoded one binade off) and checks that the pin written for that function fails on it.
+The same pins pass on the real oracle in their own modules, so together they show that the pins
+are sharp enough to catch that class of mistake."""
+import contextlib
+
+import pytest
+
+import oracle as o
+import test_oracle_bias as bias_pins
+import test_oracle_codec as codec_pins
+import test_oracle_history_gemm as history_gemm_pins
+import test_oracle_quant as quant_pins
+
+
+@contextlib.contextmanager
+def _mutant(tmp_path, old, new):
+    src = open(o._SRC).read()
+    assert src.count(old) == 1, old
+    path = tmp_path / "fp8_oracle.c"
+    path.write_text(src.replace(old, new))
+    o.lib()  # the real oracle is loaded (and built) before it is swapped out
+    saved = (o._SRC, o._LIB, o._lib)
+    o._SRC, o._LIB, o._lib = str(path), str(tmp_path / "liboracle.so"), None
+    try:
+        o.lib()
+        yield o
+    finally:
+        o._SRC, o._LIB, o._lib = saved
+
+
+MUTANTS = {
+    "ties round away from even": (
+        "else c = (lo & 1) ? hi : lo;", "else c = hi;",
+        lambda m: codec_pins.test_midpoints_tie_to_even(m, 0)),
+    "subnormals decoded one binade low": (
+        "v = ldexp((double)m, 1 - bias - mb);", "v = ldexp((double)m, -bias - mb);",
+        lambda m: codec_pins.test_decode_matches_torch_all_codes(m, 0)),
+    "compute_bias rounds instead of flooring": (
+        "long e = (long)(x - 1) - (long)margin;", "long e = (long)x - (long)margin;",
+        lambda m: bias_pins.test_bracket_property(m, 0)),
+    "margin added instead of subtracted": (
+        "long e = (long)(x - 1) - (long)margin;", "long e = (long)(x - 1) + (long)margin;",
+        lambda m: bias_pins.test_margin_shift(m, 1, 2)),
+    "history window forgets all but its first entry": (
+        "int64_t n = *pos < L ? *pos : L;", "int64_t n = 1;",
+        lambda m: history_gemm_pins.test_history_window_invariant(m, 4, 0, 0)),
+    "sampled product: block scale of B read from row 0": (
+        "\n        for (int64_t k = 0; k < K; ++k) {\n"
+        "            double a = fp8o_decode(A[m * lda + k], fa) * operand_scale(ga, sfa, m, k, K);\n"
+        "            double b = fp8o_decode(B[n * ldb + k], fb) * operand_scale(gb, sfb, n, k, K);",
+        "\n        for (int64_t k = 0; k < K; ++k) {\n"
+        "            double a = fp8o_decode(A[m * lda + k], fa) * operand_scale(ga, sfa, m, k, K);\n"
+        "            double b = fp8o_decode(B[n * ldb + k], fb) * operand_scale(gb, sfb, 0, k, K);",
+        lambda m: history_gemm_pins.test_gemm_exact_block(m, 1, 1)),
+    "whole product: block scale of B read from row 0": (
+        "                double b = fp8o_decode(B[n * ldb + k], fb) * operand_scale(gb, sfb, n, k, K);",
+        "                double b = fp8o_decode(B[n * ldb + k], fb) * operand_scale(gb, sfb, 0, k, K);",
+        lambda m: history_gemm_pins.test_gemm_full_exact_block(m, 1, 1)),
+    "whole product: MX scale of A from the wrong K block": (
+        "                double a = fp8o_decode(A[m * lda + k], fa) * operand_scale(ga, sfa, m, k, K);",
+        "                double a = fp8o_decode(A[m * lda + k], fa) * operand_scale(ga, sfa, m, k ^ 32, K);",
+        lambda m: history_gemm_pins.test_gemm_full_exact_block(m, 3, 3)),
+    "column-wise copy written in reverse row order": (
+        "if (q_col) q_col[j * rows + i] = (uint8_t)code;", "if (q_col) q_col[j * rows + (rows - 1 - i)] = (uint8_t)code;",
+        lambda m: quant_pins.test_tensor_quant_brute_force(m, 0)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pin_catches_planted_mistake(tmp_path, name):
+    old, new, pin = MUTANTS[name]
+    with _mutant(tmp_path, old, new) as m:
+        with pytest.raises(AssertionError):
+            pin(m)
+    pin(o)  # and the real oracle passes the same pin
