@@ -54,6 +54,16 @@ def test_history_nonfinite(oracle):
     assert st.bias[0] == 0
 
 
+def test_history_nan_stays_in_window(oracle):
+    """A NaN amax is flagged and gives e = 0 for as long as it stays in the window (L = 3 steps)."""
+    st = oracle.HistoryState(3)
+    assert not st.update(2.0, 0, 0)
+    flags = [st.update(v, 0, 0) for v in (float("nan"), 1.0, 1.0)]
+    assert flags == [True, True, True] and st.bias[0] == 0  # NaN recorded at step 1, still in the window
+    assert not st.update(1.0, 0, 0)  # overwritten: window {1, 1, 1}
+    assert st.bias[0] == oracle.compute_bias(1.0, 0, 0)[0] == 8
+
+
 def test_delayed_activation_sequence(oracle):
     """The growing-activation sequence (1 + 0.1 t) at a reduced 512x512 size: after each step the
     bias is compute_bias of the window max, recomputed here from numpy amaxes."""

@@ -1,7 +1,9 @@
 """Planted mistakes in the oracle: each case compiles a copy of the oracle's C source with one
-plausible mistake (a wrong tie rule, an off-by-one exponent, a flipped margin sign, a window that
-forgets its history, a scale read from the wrong row, a column-wise copy in the wrong order, a
-subnormal decoded one binade off) and checks that the pin written for that function fails on it.
+plausible mistake (a wrong tie rule, an off-by-one exponent or E8M0 code, a flipped margin sign, a
+window that forgets its history or a NaN, a block amax over part of its block, a scale read from the
+wrong row or K block, a column-wise copy in the wrong order, a subnormal decoded one binade off, a
+statistic that counts zeros, a cast that drops its scale) and checks that the pin written for that
+function fails on it.
 The same pins pass on the real oracle in their own modules, so together they show that the pins
 are sharp enough to catch that class of mistake."""
 import contextlib
@@ -9,10 +11,13 @@ import contextlib
 import pytest
 
 import oracle as o
+import test_oracle_alternatives as alternative_pins
 import test_oracle_bias as bias_pins
 import test_oracle_codec as codec_pins
+import test_oracle_f32cast as f32cast_pins
 import test_oracle_history_gemm as history_gemm_pins
 import test_oracle_quant as quant_pins
+import test_oracle_stats as stats_pins
 
 
 @contextlib.contextmanager
@@ -63,6 +68,31 @@ MUTANTS = {
         "                double a = fp8o_decode(A[m * lda + k], fa) * operand_scale(ga, sfa, m, k, K);",
         "                double a = fp8o_decode(A[m * lda + k], fa) * operand_scale(ga, sfa, m, k ^ 32, K);",
         lambda m: history_gemm_pins.test_gemm_full_exact_block(m, 3, 3)),
+    "amax drops a NaN": (
+        "            if (isnan(a) || a > m) m = a;", "            if (a > m) m = a;",
+        lambda m: quant_pins.test_amax_matches_numpy(m)),
+    "history window drops a NaN": (
+        "if (isnan(hist[i]) || hist[i] > m) m = hist[i];", "if (hist[i] > m) m = hist[i];",
+        lambda m: history_gemm_pins.test_history_nan_stays_in_window(m)),
+    "128x128 block amax taken over its first row only": (
+        "float amax = amax_of(x + i0 * rs + j0 * cs, ni, nj, rs, cs);", "float amax = amax_of(x + i0 * rs + j0 * cs, 1, nj, rs, cs);",
+        lambda m: quant_pins.test_block_quant_brute_force(m, 2, 0, (130, 96))),
+    "E8M0 code off by one": (
+        "sf_e8m0[b] = (uint8_t)(127 - e);", "sf_e8m0[b] = (uint8_t)(128 - e);",
+        lambda m: quant_pins.test_block_quant_brute_force(m, 3, 0, (3, 160))),
+    "OCP bias one binade off": (
+        "long e = (long)(fmt == FMT_E4M3 ? 8 : 15) - (long)(x - 1) - (long)margin;",
+        "long e = (long)(fmt == FMT_E4M3 ? 8 : 15) - (long)x - (long)margin;",
+        lambda m: alternative_pins.test_ocp_hand_values(m, 0, 448.0, 0)),
+    "ratio scale through a rounded reciprocal": (
+        "(float)fmt_max(fmt) / a;", "(float)fmt_max(fmt) * (1.0f / a);",
+        lambda m: alternative_pins.test_ratio_scale_correctly_rounded(m, 0)),
+    "flush-to-zero count includes the zeros": (
+        "if (xv != 0.0f && (fp8o_encode(v, fmt) & 0x7F) == 0) ++und;", "if ((fp8o_encode(v, fmt) & 0x7F) == 0) ++und;",
+        lambda m: stats_pins.test_nan_and_zero_count_in_neither(m)),
+    "fp32 cast ignores its scale": (
+        "        float p = x[i] * s;", "        float p = x[i];",
+        lambda m: f32cast_pins.test_matches_torch_in_range(m, 0, 0.3)),
     "column-wise copy written in reverse row order": (
         "if (q_col) q_col[j * rows + i] = (uint8_t)code;", "if (q_col) q_col[j * rows + (rows - 1 - i)] = (uint8_t)code;",
         lambda m: quant_pins.test_tensor_quant_brute_force(m, 0)),
