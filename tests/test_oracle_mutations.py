@@ -106,3 +106,32 @@ def test_pin_catches_planted_mistake(tmp_path, name):
         with pytest.raises(AssertionError):
             pin(m)
     pin(o)  # and the real oracle passes the same pin
+
+
+# The bf16 rounding and the output-cast bracket are Python functions of the oracle: the mistake is
+# planted in the function's own source, which is executed in the oracle module's namespace.
+PY_MUTANTS = {
+    "bf16 rounding truncates": (
+        "round_bf16", "r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16", "r = (u >> 16) << 16",
+        lambda m: history_gemm_pins.test_round_bf16_matches_torch(m)),
+    "output-cast bracket starts at the nearest code": (
+        "gemm_quantize_bracket", "return codes(y_ref - tol), codes(y_ref + tol), codes(y_ref)",
+        "return codes(y_ref), codes(y_ref + tol), codes(y_ref)",
+        lambda m: history_gemm_pins.test_gemm_quantize_bracket_brute_force(m, 0)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_pin_catches_planted_mistake_in_python(monkeypatch, name):
+    import inspect
+    import textwrap
+    fn, old, new, pin = PY_MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(getattr(o, fn)))
+    assert src.count(old) == 1, old
+    ns = dict(vars(o))
+    exec(compile(src.replace(old, new), f"<mutant {fn}>", "exec"), ns)
+    monkeypatch.setattr(o, fn, ns[fn])
+    with pytest.raises(AssertionError):
+        pin(o)
+    monkeypatch.undo()
+    pin(o)
