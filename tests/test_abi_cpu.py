@@ -228,3 +228,22 @@ def test_history_batch_validation(L):
         setattr(recs[1], field, bad)
         assert f(addr, 2, None) == 1, field
         setattr(recs[1], field, good)
+
+
+def test_binding_argument_counts_match_the_header(L):
+    """Every entry point's ctypes argument list has as many entries as its declaration has
+    parameters (the binding and the header cannot drift apart unnoticed)."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    decls = dict(re.findall(r"FP8Q_API\s+[^;(]*?\b(fp8_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", text))
+    import scaling_quantization_gemm_gb300 as q
+    q.lib()
+    checked = 0
+    for name in q.ENTRY_POINTS:
+        params = decls[name].strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        argtypes = getattr(L, name).argtypes
+        if argtypes is None:
+            continue
+        assert len(argtypes) == n, (name, len(argtypes), n)
+        checked += 1
+    assert checked >= 12
