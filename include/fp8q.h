@@ -20,8 +20,9 @@
  *   - Every pointer argument that names a tensor is a DEVICE pointer into memory
  *     the caller allocated and owns.  The library allocates no device memory and
  *     keeps no state between calls (the one exception is the static scratch of
- *     fp8_quantize_current_noalloc); it is safe to call from several host
- *     threads on different streams.
+ *     fp8_quantize_current_noalloc).  Every entry point except
+ *     fp8_quantize_current_noalloc is safe to call from several host threads on
+ *     different streams; calls of that one must be ordered on the GPU.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
  *     only enqueues work on that stream and returns; none synchronises the host.
  *   - Arguments are validated on the host before anything is enqueued:
@@ -344,8 +345,8 @@ FP8Q_API fp8_status fp8_quantize_current(const void *x, int64_t rows, int64_t co
  * Arguments and results are those of fp8_quantize_current, without
  * `workspace`.  The scratch is a static 4 KB array in the library's device
  * code, present on every GPU that loads the library until the process exits.
- * It holds one slot per CTA, at most 1020 CTAs; a launch that would need more
- * returns FP8_ERR_UNSUPPORTED.
+ * It holds one slot per CTA, so the launch uses at most 1020 CTAs (fewer than
+ * would fit on a GPU with more resident CTAs; GB300 uses 456).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make that
  *     first call before any stream capture.
@@ -381,16 +382,18 @@ FP8Q_API fp8_status fp8_quantize_current_noalloc(const void *x, int64_t rows, in
  *              otherwise neither may be TENSOR, and each of sfa / sfb is
  *                1x128:   fp32 [rows x ceil(K/128)]
  *                128x128: fp32 [ceil(rows/128) x ceil(K/128)]
- *                MX 1x32: u8 E8M0 [rows x ceil(K/32)] (K must be a multiple of 32;
- *                  fp8_quantize writes codes 0..253; code 255, NaN in the OCP
- *                  MX encoding, gives an unspecified result)
+ *                MX 1x32: u8 E8M0 [rows x K/32] (fp8_quantize writes codes
+ *                  0..253; code 255, NaN in the OCP MX encoding, gives an
+ *                  unspecified result)
  *              (rows = M for A, N for B).  fp32 block scales must be powers of
  *              two in [2^-127, 2^127] (what fp8_quantize writes); any other
  *              value sets FP8_STATUS_BAD_BLOCK_SCALE.
  *   D        device, [M x N] fp32 or bf16 (out_dtype), leading dimension ldd
  *            (elements); 16-byte aligned, N and ldd multiples of 16.
  *   status   device int32 or NULL (FP8_STATUS_TIMEOUT, FP8_STATUS_BAD_BLOCK_SCALE).
- * K == 0 writes zeros.  Block-scaled modes need M, N >= 1 and K >= 32.
+ * K == 0 writes zeros.  Every block-scaled mode (1x128, 128x128 and MX 1x32
+ * alike) needs K % 128 == 0 (one 128-wide K tile per scale load) and 4-byte
+ * aligned sfa / sfb; other K return FP8_ERR_UNSUPPORTED.
  */
 FP8Q_API fp8_status fp8_scaled_gemm(fp8_gemm_op op, int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda,
                            fp8_format fa, fp8_granularity ga, const void *sfa, const uint8_t *B, int64_t ldb,

@@ -116,6 +116,17 @@ def test_gemm_validation(L):
     assert g(*args(M=0)) == 0  # empty output: no-op
 
 
+def test_block_scaled_k_rule_matches_the_header(L):
+    """The header states that every block-scaled mode needs K % 128 == 0; the check returns
+    FP8_ERR_UNSUPPORTED for K = 32, 64, 96 and 160 in each mode (MX 1x32 included)."""
+    text = " ".join(w for line in open(HEADER) for w in line.strip().lstrip("*").split())
+    assert "Every block-scaled mode (1x128, 128x128 and MX 1x32 alike) needs K % 128 == 0" in text
+    g = L.fp8_scaled_gemm
+    for ga, gb in ((3, 3), (1, 2), (1, 1), (2, 2), (4, 4)):
+        for K in (32, 64, 96, 160):
+            assert g(0, 256, 256, K, FAKE, 256, 0, ga, FAKE, FAKE, 256, 0, gb, FAKE, FAKE, 1, 256, None, None) == 2
+
+
 def test_quantize_current_validation(L):
     qc = L.fp8_quantize_current
     a = lambda **kw: [kw.get("x", FAKE), kw.get("rows", 32), kw.get("cols", 32), kw.get("ld", 32), kw.get("fmt", 0),
