@@ -753,7 +753,12 @@ __global__ void __launch_bounds__(320, 1)
 // B row n: lane 32q + n%32, column 8 + n/32, every quarter q).  The producer
 // TMA-loads the scales of each group of four K tiles (16 bytes per row: the A
 // rows of this CTA and all B rows of the tile) into a four-slot shared-memory
-// ring, two groups ahead; the writers read them there.  TMEM has room for four
+// ring, two groups ahead.  When a group lands, each writer thread reads the
+// words of its rows for the group's four K tiles into registers -- E8M0 words
+// as they are; power-of-two fp32 block scales (1x128, 128x128) re-encoded as
+// E8M0 and repeated over the four 32-wide sub-blocks -- and frees the slot, so
+// what a writer does after waiting for a TMEM slot is the same few stores for
+// every scale kind.  TMEM has room for four
 // scale slots (64 columns beside the two 224-column accumulators): K tile i
 // (counted over all of a pair's tiles) uses stage i / 2 % 3 and scale slot
 // i % 4.  The even CTA's `full[stage]` completes when both producers' loads
@@ -794,15 +799,24 @@ __host__ __device__ constexpr int scale_box_rows(int rows) {
     return KIND == SF_BLOCK ? (rows == kPairRows ? 1 : kScaleBlockRowsB) : rows;
 }
 
-// Scale word (four E8M0 bytes) of local row r, K tile jj of the group, from the shared-memory slot.
+// The scale words of one operand row for the four K tiles of a scale group (word jj: four E8M0 bytes,
+// one per 32-wide K sub-block of K tile jj), from the group's shared-memory slot: MX words as they
+// are, fp32 block scales re-encoded (a value that is not a power of two sets `bad`).  Local row r of
+// the slot, or for 128x128 scales the block row of `row` counted from `block_base`; rows past the
+// edge get the neutral scale 1.
 template <int KIND>
-__device__ __forceinline__ uint32_t sf_word_smem(const uint8_t* slot, int r, int jj, int block_base, int64_t row,
-                                                 int64_t rows, uint32_t& bad) {
-    if (row >= rows) return 0x7F7F7F7Fu;
-    if constexpr (KIND == SF_MX) return *reinterpret_cast<const uint32_t*>(slot + r * 16 + 4 * jj);
-    const int br = KIND == SF_ROW ? r : (int)(row >> 7) - block_base;
-    const float f = reinterpret_cast<const float*>(slot)[br * 4 + jj];
-    return e8m0_of_pow2(f, bad) * 0x01010101u;
+__device__ __forceinline__ void sf_group_words(const uint8_t* slot, int r, int block_base, int64_t row, int64_t rows,
+                                               uint32_t (&w)[4], uint32_t& bad) {
+    if (row >= rows) {
+        w[0] = w[1] = w[2] = w[3] = 0x7F7F7F7Fu;
+        return;
+    }
+    const int sr = KIND == SF_BLOCK ? (int)(row >> 7) - block_base : r;
+    const uint4 v = *reinterpret_cast<const uint4*>(slot + sr * 16);
+    const uint32_t raw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+        w[jj] = KIND == SF_MX ? raw[jj] : e8m0_of_pow2(__uint_as_float(raw[jj]), bad) * 0x01010101u;
 }
 
 template <int OUT_BF16, int KA, int KB>
@@ -822,9 +836,7 @@ __global__ void __launch_bounds__(320, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBsPairStages; ++s) {
-            // both producers + the eight scale writers of the pair, once per stage (MX) or per K tile
-            // both producers + the eight scale writers of the pair, once per stage (MX) or per K tile
-            mbar_init(smem_u32(&S.full[s]), 2 + 8 * ((KA == SF_MX && KB == SF_MX) ? 1 : kBsKPerStage));
+            mbar_init(smem_u32(&S.full[s]), 2 + 8);  // both producers + the eight scale writers of the pair
             mbar_init(smem_u32(&S.empty[s]), 1);     // the MMA commit
         }
         for (int s = 0; s < kScaleSlots; ++s) {
@@ -984,9 +996,11 @@ __global__ void __launch_bounds__(320, 1)
             if (acc == 0) acc_phase ^= 1;
         }
     } else {
-        // Scale writers of this CTA (warp 6..9 = lane quarter q): for every K tile, the A scale of rows
-        // 32q + lane (column q of the K tile's slot) and the scales of all 224 B rows (columns 8 + j),
-        // read from the shared-memory scale ring (k_tiles is a multiple of 4 on this path).
+        // Scale writers of this CTA (warp 6..9 = lane quarter q): for every K tile, the A scale of row
+        // 32q + lane (column q of the K tile's slot) and the scales of all 224 B rows (columns 8 + j).
+        // When a group's scales land, each thread reads the words of its rows for the group's four K
+        // tiles into registers (re-encoding fp32 block scales there) and frees the ring slot; after
+        // each slot wait only the TMEM stores remain, the same for every scale kind.
         const int q = warp & 3;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int kcount = 0;  // K tiles written so far (over all of this pair's tiles)
@@ -999,20 +1013,26 @@ __global__ void __launch_bounds__(320, 1)
             const int64_t arow = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows + q * 32 + lane;
             const int ablock = (tm * kPairTile + (int)rank * kPairRows) >> 7;
             const int bblock = (tn * BN_BS) >> 7;
-            for (int grp = 0; ok && grp < groups; ++grp) {
+            for (int grp = 0; ok && grp < groups; ++grp) {  // k_tiles is a multiple of 4 on this path
                 const int slot = consumed % kScaleSlots;
-                bool w = mbar_wait_bounded(smem_u32(&S.scale_full[slot]), (uint32_t)((consumed / kScaleSlots) & 1), abort_flag);
+                bool w = mbar_wait_bounded(smem_u32(&S.scale_full[slot]), (uint32_t)((consumed / kScaleSlots) & 1),
+                                           abort_flag);
                 if (!__all_sync(0xffffffffu, w)) {
                     ok = false;
                     break;
                 }
-                // MX scales are copied as they are and both K tiles of a stage go out after one wait
-                // (2.23 -> 2.11 ms on 16384x28672x8192); fp32 block scales are re-encoded first, and there
-                // each K tile going out on its own is faster (0.29 against 0.32 ms on 8192x11008x4096)
-                constexpr int kPer = (KA == SF_MX && KB == SF_MX) ? kBsKPerStage : 1;  // K tiles per arrival
+                uint32_t wa[4], wb[kSfbCols][4];
+                sf_group_words<KA>(S.sa[slot], q * 32 + lane, ablock, arow, g.M, wa, bad);
 #pragma unroll
-                for (int u = 0; u < 4 / kPer; ++u) {
-                    if (kcount >= kSfSlots) {  // the MMAs of K tile kcount - 4 (and - 3) are done with the slots
+                for (int j = 0; j < kSfbCols; ++j)
+                    sf_group_words<KB>(S.sb[slot], 32 * j + lane, bblock, (int64_t)tn * BN_BS + 32 * j + lane, g.N,
+                                       wb[j], bad);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.scale_empty[slot]));  // the producer may refill the slot
+                ++consumed;
+#pragma unroll
+                for (int u = 0; u < 4 / kBsKPerStage; ++u) {  // one stage (two K tiles) per arrival
+                    if (kcount >= kSfSlots) {  // the MMAs of K tiles kcount - 4 and - 3 are done with the slots
                         const int prev = (kcount - kSfSlots) / kBsKPerStage;  // the stage step that held them
                         w = mbar_wait_bounded(smem_u32(&S.empty[prev % kBsPairStages]),
                                               (uint32_t)((prev / kBsPairStages) & 1), abort_flag);
@@ -1024,29 +1044,23 @@ __global__ void __launch_bounds__(320, 1)
                     tc_fence_after();
                     const int stage = (kcount / kBsKPerStage) % kBsPairStages;
 #pragma unroll
-                    for (int h = 0; h < kPer; ++h) {
-                        const int jj = kPer * u + h;
+                    for (int h = 0; h < kBsKPerStage; ++h) {
+                        const int jj = kBsKPerStage * u + h;
                         const uint32_t tslot =
                             tmem + lane_base + (uint32_t)(kSfColBase + ((kcount + h) % kSfSlots) * kSfColsPerStage);
-                        tmem_st_32x32b_x1(tslot + q,
-                                          sf_word_smem<KA>(S.sa[slot], q * 32 + lane, jj, ablock, arow, g.M, bad));
-                        uint32_t wb[8];
+                        tmem_st_32x32b_x1(tslot + q, wa[jj]);
+                        uint32_t v8[8];
 #pragma unroll
-                        for (int j = 0; j < kSfbCols; ++j)
-                            wb[j] = sf_word_smem<KB>(S.sb[slot], 32 * j + lane, jj, bblock,
-                                                     (int64_t)tn * BN_BS + 32 * j + lane, g.N, bad);
-                        wb[7] = 0x7F7F7F7Fu;
-                        tmem_st_32x32b_x8(tslot + 8, wb);
+                        for (int j = 0; j < kSfbCols; ++j) v8[j] = wb[j][jj];
+                        v8[7] = 0x7F7F7F7Fu;
+                        tmem_st_32x32b_x8(tslot + 8, v8);
                     }
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&S.full[stage]), 0));
-                    kcount += kPer;
+                    kcount += kBsKPerStage;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&S.scale_empty[slot]));
-                ++consumed;
             }
         }
         if (__any_sync(0xffffffffu, bad != 0) && lane == 0) atomicOr(&S.bad_scale, 1);
