@@ -68,18 +68,87 @@ def make_inputs():
 
 # ------------------------------------------------------------- GPU side
 
+class Nvml:
+    """The few NVML queries the clock record needs, through ctypes (no Python NVML package on the GPU
+    hosts).  `handle(i)` is None where NVML cannot be loaded."""
+
+    SM = 1  # NVML_CLOCK_SM
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            self.ok = self.lib.nvmlInit_v2() == 0
+        except OSError:
+            self.lib, self.ok = None, False
+
+    def handle(self, cuda_index: int):
+        """NVML handle of the CUDA device: by UUID where torch reports it, else the CUDA index mapped
+        through CUDA_VISIBLE_DEVICES."""
+        if not self.ok:
+            return None
+        c = self.c
+        h = c.c_void_p()
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            if self.lib.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), c.byref(h)) == 0:
+                return h
+        except (AttributeError, RuntimeError, AssertionError):
+            pass
+        idx = cuda_index
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+        if cuda_index < len(vis) and vis[cuda_index].strip().isdigit():
+            idx = int(vis[cuda_index])
+        return h if self.lib.nvmlDeviceGetHandleByIndex_v2(c.c_uint(idx), c.byref(h)) == 0 else None
+
+    def sample_line(self, h, index: int) -> str:
+        """One sample in the CSV fields of ClockSampler.FIELDS."""
+        c = self.c
+        clk, mx, mw, rs = c.c_uint(), c.c_uint(), c.c_uint(), c.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(h, self.SM, c.byref(clk))
+        self.lib.nvmlDeviceGetMaxClockInfo(h, self.SM, c.byref(mx))
+        self.lib.nvmlDeviceGetPowerUsage(h, c.byref(mw))
+        self.lib.nvmlDeviceGetCurrentClocksEventReasons(h, c.byref(rs))
+        act = lambda bit: "Active" if rs.value & bit else "Not Active"
+        # reason bits: 0x4 sw power cap, 0x8 hw slowdown, 0x20 sw thermal, 0x40 hw thermal
+        return (f"{index}, {clk.value}, {mx.value}, {mw.value / 1000.0:.2f}, 0x{rs.value:x}, {act(0x8)}, "
+                f"{act(0x40)}, {act(0x20)}, {act(0x4)}")
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
+    """SM clock, power and throttle-reason samples during the timed region: NVML every 10 ms from a
+    thread of this process (nvidia-smi every 50 ms where NVML cannot be loaded).  NVML refreshes the
+    clock it reports only every few tens of ms, so a sample can lag the clock by that much."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.01
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.thread = None
+        self.lines = []
 
     def __enter__(self):
+        import threading
+        self.lines = []
+        nv = Nvml()
+        h = nv.handle(self.gpu)
+        if h is not None:
+            self.stop = threading.Event()
+
+            def run():
+                while not self.stop.is_set():
+                    self.lines.append(nv.sample_line(h, self.gpu))
+                    self.stop.wait(self.PERIOD_S)
+
+            self.thread = threading.Thread(target=run, daemon=True)
+            self.thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "50"],
@@ -89,7 +158,10 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join()
+            return
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -211,16 +283,33 @@ def run_ours(args, rank, world):
             torch.cuda.synchronize()
         barrier(world)
         total = max_over_ranks(start.elapsed_time(end), world)
-        ops_ms = {ops[i][0]: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
-                  for i in range(nops)}
-        return total, ops_ms, sampler.summary()
+        op_ms = lambda s, i: evs[s][i].elapsed_time(evs[s][i + 1])
+        ops_ms = {ops[i][0]: statistics.mean(op_ms(s, i) for s in range(args.steps)) for i in range(nops)}
+        # the software power cap lowers the SM clock once the GPU has drawn its limit for some tens of
+        # ms: the first timed step runs before it bites, the last ones under it
+        late = range(max(1, args.steps - 5), args.steps)
+        cap = {"first_step_ms": {ops[i][0]: round(op_ms(0, i), 4) for i in range(nops) if ops[i][2] != "other"},
+               "last_steps_ms": ({ops[i][0]: round(statistics.mean(op_ms(s, i) for s in late), 4)
+                                  for i in range(nops) if ops[i][2] != "other"} if len(late) else None)}
+        return total, ops_ms, sampler.summary(), cap
 
-    total_ms, per_op, clock_summary = timed()
+    total_ms, per_op, clock_summary, power_cap = timed()
     suspect = clock_suspect(clock_summary)
     if max_over_ranks(1.0 if suspect else 0.0, world) > 0:
-        total_ms, per_op, clock_summary = timed()
+        total_ms, per_op, clock_summary, power_cap = timed()
         clock_summary["remeasured_after"] = suspect or ["another rank"]
     ms_step = total_ms / args.steps
+
+    # the same steps without the per-op events (they cost the step nothing measurable)
+    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    a_ev.record(stream)
+    for _ in range(args.steps):
+        step()
+    b_ev.record(stream)
+    torch.cuda.synchronize()
+    power_cap["ms_per_step_without_op_events"] = round(max_over_ranks(a_ev.elapsed_time(b_ev), world) / args.steps, 3)
     status = [int(c4.status.item()), int(c3.status.item())] + [int(s.status.item()) for s in (c5.sx, c5.sw, c5.sg)]
 
     # --- end to end: pinned host inputs in, results out, every step ---
@@ -238,9 +327,13 @@ def run_ours(args, rank, world):
     quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9
     value = step_flops * world / (ms_step * 1e-3) / 1e12
     traffic = load_traffic("gemm_tensor_pair_kernel")
+    prof = load_profile_record("gemm_tensor_pair_kernel")
     peak_note = f"{'sustained' if long_loop else 'burst'} bf16 x {FP8_OVER_BF16:g} (nominal fp8/bf16), {pk_src}"
 
     nxt = measure_next_rows(args, dev, c5, pk, stream) if not args.no_next_rows else None
+    # context for the FP8 peak (2 x the measured bf16 cuBLAS figure): the library FP8 GEMM on the fprop
+    # operands, measured here, and the committed ncu tensor-pipe activity of the fprop launch
+    lib_fp8 = cublaslt_fp8_tflops(c5.qx_row, c5.qw_row, c5.sx.scale_inv, c5.sw.scale_inv)
 
     cpu = cpu_baseline(host, step_flops) if (rank == 0 and not args.no_cpu_baseline) else None
     line = {
@@ -257,7 +350,12 @@ def run_ours(args, rank, world):
                      # context: the step runs under the power cap, where the measured sustained bf16
                      # figure (a seconds-long cuBLAS loop) is the like-for-like denominator
                      "frac_of_sustained": round(
-                         tensor_tflops / (pk["bf16_tflops_sustained"] * FP8_OVER_BF16), 4)},
+                         tensor_tflops / (pk["bf16_tflops_sustained"] * FP8_OVER_BF16), 4),
+                     # the peak is not a measured FP8 figure: beside it, the kernel's tensor-pipe
+                     # activity from ncu (standalone launch) and cuBLASLt FP8 on the same operands
+                     "ncu_tensor_pipe_active": (float(prof["tensor_pipe_active"])
+                                                if "tensor_pipe_active" in prof else None),
+                     "cublaslt_fp8_tflops_same_shape": lib_fp8},
         "roofline_quantizer": {"bound": "hbm", "kernel": "quantize_tile_kernel (all casts of the step)",
                                "achieved": round(quant_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                                "frac": round(quant_gbs / pk["hbm_gbs"], 4), "peak_source": pk_src,
@@ -267,6 +365,7 @@ def run_ours(args, rank, world):
                                  "per_block_tflops": round(blk_tflops, 1),
                                  "per_block_frac": round(blk_tflops / fp8_peak, 4)},
         "breakdown_ms": {k: round(v, 4) for k, v in per_op.items()},
+        "power_cap": power_cap,
         "next_rows": nxt,
         "device_status": status,
         "e2e": e2e,
@@ -295,7 +394,8 @@ def _time_op(f, reps: int, stream, warmup: int = 3) -> float:
 
 def measure_next_rows(args, dev, c5, pk, stream):
     """The rows beyond the training step, each on its own, outside the timed step: the fused
-    current-scaling cast, the fixed-bias (FP8-CSCALE) sweep statistics, and post-training-quantised
+    current-scaling cast, the fixed-bias (FP8-CSCALE) sweep statistics, the 16-iteration delayed-scaling
+    workload (activation and gradient casts with their history updates), and post-training-quantised
     inference through two FP8 linear layers with the hidden cast fused into GEMM 1's epilogue."""
     import torch
 
@@ -333,9 +433,40 @@ def measure_next_rows(args, dev, c5, pk, stream):
                                  "frac": round(gbs / hbm, 4), "bytes_per_elem": 2,
                                  "underflow_frac_by_e": {r["e"]: round(r["underflow_frac"], 6) for r in sweep}}
 
+    # delayed scaling over 16 iterations: a 4096 x 4096 activation N(0, 1) (1 + 0.1 t) in E4M3 (margin 0)
+    # and a 4096 x 4096 gradient Laplace(0, 1e-4) in E5M2 (margin 1), history length 16.  Each iteration
+    # casts both row-wise with the scale the history gives and the fused amax, then updates both
+    # histories in one launch.  The 32 distinct inputs (1 GB) exceed L2, so a pass needs no flush;
+    # 3 B per element and tensor (2 B read, 1 B written)
+    from scaling_quantization_gemm_gb300.step import ScaleState, current_scaling
+    to = lambda b: torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
+    acts = [to(wl.delayed_activation(t)) for t in range(16)]
+    grads = [to(wl.delayed_gradient(t)) for t in range(16)]
+    sa, sg = ScaleState(q.E4M3, 0, 16, dev), ScaleState(q.E5M2, 1, 16, dev)
+    qa = torch.empty(4096, 4096, dtype=torch.uint8, device=dev)
+    qg = torch.empty_like(qa)
+    current_scaling(acts[0], sa)  # the first iteration's scale comes from its own amax (empty history)
+    current_scaling(grads[0], sg)
+
+    def delayed_pass():
+        for t in range(16):
+            q.fp8_quantize(acts[t], q.E4M3, q.TENSOR, scale=sa.scale, q_row=qa, amax=sa.amax)
+            q.fp8_quantize(grads[t], q.E5M2, q.TENSOR, scale=sg.scale, q_row=qg, amax=sg.amax)
+            q.fp8_amax_history_update_batch((sa, sg))
+
+    ms = _time_op(delayed_pass, 10, stream)
+    nbytes = 16 * 2 * 3.0 * 4096 * 4096
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["delayed_scaling_16_iterations"] = {
+        "kernel": "quantize_tile_kernel<TENSOR> (E4M3 and E5M2, row-wise, fused amax) + history_batch_kernel",
+        "shape": [4096, 4096], "iterations": 16, "history_len": 16, "launches_per_pass": 48,
+        "ms_per_pass": round(ms, 4), "achieved": round(gbs, 1), "unit": "GB/s", "peak": hbm,
+        "frac": round(gbs / hbm, 4), "bytes_per_elem": 3,
+        "status": [int(sa.status.item()), int(sg.status.item())]}
+    del acts, grads
+
     # PTQ inference: 8192 tokens through 5120 -> 13824 -> 5120, hidden cast in GEMM 1's epilogue
     Xb, W1b, W2b = wl.ptq_ffn()
-    to = lambda b: torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
     Xd = to(Xb)
     stack = PTQStack(to(W1b), to(W2b), Xb.shape[0], act="current")
     stack.forward(Xd)  # first forward: no hidden history yet (bf16 GEMM 1 + current scaling)
@@ -423,22 +554,44 @@ def run_e2e(args, d, host, ops, stream, c1, c5, c4, c3, step_flops, world):
             "steps": steps, "copies": "overlapped with compute (double-buffered, two copy streams)"}
 
 
-def load_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` at the benchmark shape, from the committed ncu summary
-    (profiles/traffic.txt), or None when the kernel source has changed since it was captured."""
+def load_profile_record(kernel: str) -> dict:
+    """The committed ncu record of `kernel` at the benchmark shape (profiles/traffic.txt): DRAM bytes per
+    launch and tensor-pipe activity, as a dict, or {} when the kernel source has changed since the
+    capture (the figures would describe other code)."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
-        return None
+        return {}
     for line in open(p):
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
         if f.get("kernel") != kernel:
             continue
         src = os.path.join(ROOT, "scaling_quantization_gemm_gb300", "csrc", f.get("source", ""))
         if not os.path.exists(src) or hashlib.sha1(open(src, "rb").read()).hexdigest() != f.get("source_sha1"):
-            return None
-        return int(f["bytes_per_launch"])
-    return None
+            return {}
+        return f
+    return {}
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from its profile record, or None (no record, or a stale one)."""
+    f = load_profile_record(kernel)
+    return int(f["bytes_per_launch"]) if "bytes_per_launch" in f else None
+
+
+def cublaslt_fp8_tflops(A8: "torch.Tensor", B8: "torch.Tensor", sa, sb, reps: int = 10):
+    """TFLOP/s of the library FP8 GEMM (torch._scaled_mm, cuBLASLt) on the same E4M3 operands and bf16
+    output, outside the timed step: a comparison for the per-tensor kernel, never part of the path.
+    None where the installed torch cannot run it."""
+    import torch
+    try:
+        a = A8.view(torch.float8_e4m3fn)
+        b = B8.view(torch.float8_e4m3fn).t()
+        f = lambda: torch._scaled_mm(a, b, scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+        ms = _time_op(f, reps, torch.cuda.current_stream())
+    except (RuntimeError, AttributeError, TypeError):
+        return None
+    return round(2.0 * A8.shape[0] * B8.shape[0] * A8.shape[1] / (ms * 1e-3) / 1e12, 1)
 
 
 # ------------------------------------------------------------- CPU oracle
