@@ -280,6 +280,42 @@ FP8Q_API fp8_status fp8_quantize(const void *x, int64_t rows, int64_t cols, int6
                         void *sf_row, void *sf_col, float *amax, void *stream);
 
 /*
+ * fp8_quantize_batch -- several fp8_quantize casts in one launch.
+ * Source: the casts of one FP8 linear layer's operands (activations and weights,
+ * and the gradient in the backward pass), each with its own scale ("Training
+ * and inference of large language models using 8-bit floating point",
+ * "Proposed method"; per-block scales: "Per-Tensor and Per-Block Scaling
+ * Strategies for Effective FP8 Training", "Key Questions Answered").
+ *
+ *   descs    HOST array of n descriptors; each names one cast with exactly the
+ *            arguments of fp8_quantize (device pointers, sizes, format,
+ *            granularity, margin) and `reserved` = 0.  Formats and granularities
+ *            may differ between descriptors.
+ *   n        0 .. FP8_QUANTIZE_BATCH_MAX; n = 0 is a no-op.
+ * Every output (codes, scales, amax) equals that of the n fp8_quantize calls
+ * made one after another; an amax shared by several descriptors accumulates
+ * the maximum over all of them.  The casts run concurrently, so no output may
+ * overlap another descriptor's input or output.  Each descriptor is validated
+ * as fp8_quantize validates its arguments, and nothing is launched unless all
+ * are valid (the error detail names the descriptor).  The grid is split among
+ * the tensors in proportion to their 128x128 tiles.
+ */
+#define FP8_QUANTIZE_BATCH_MAX 4
+typedef struct fp8_quantize_desc {
+    const void *x;   /* bf16 [rows x cols], leading dimension ld (elements) */
+    int64_t rows, cols, ld;
+    int32_t fmt;      /* fp8_format */
+    int32_t gran;     /* fp8_granularity */
+    int32_t margin;
+    int32_t reserved; /* must be 0 */
+    const float *scale;
+    uint8_t *q_row, *q_col;
+    void *sf_row, *sf_col;
+    float *amax;
+} fp8_quantize_desc;
+FP8Q_API fp8_status fp8_quantize_batch(const fp8_quantize_desc *descs, int32_t n, void *stream);
+
+/*
  * fp8_quantize_f32 -- the per-tensor scaled cast of an fp32 tensor.
  * Source: the scaling step that precedes the FP8 cast ("Training and
  * inference of large language models using 8-bit floating point", "Proposed

@@ -34,7 +34,8 @@ STATUS_NONFINITE_AMAX, STATUS_TIMEOUT, STATUS_BAD_BLOCK_SCALE = 1, 2, 4
 # every entry point declared in include/fp8q.h
 ENTRY_POINTS = ("fp8_amax", "fp8_compute_scale", "fp8_compute_scale_ratio", "fp8_amax_history_update",
                 "fp8_amax_history_update_batch",
-                "fp8_set_bias", "fp8_cast_stats", "fp8_quantize", "fp8_quantize_f32", "fp8_quantize_current",
+                "fp8_set_bias", "fp8_cast_stats", "fp8_quantize", "fp8_quantize_batch", "fp8_quantize_f32",
+                "fp8_quantize_current",
                 "fp8_quantize_current_noalloc",
                 "fp8_scaled_gemm", "fp8_scaled_gemm_quantize", "fp8_status_string", "fp8_last_error_detail")
 QUANTIZE_CURRENT_WORKSPACE_BYTES = 4096  # FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES
@@ -67,6 +68,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_amax_history_update": [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp],
                 "fp8_amax_history_update_batch": [vp, i32, vp],
                 "fp8_quantize": [vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp],
+                "fp8_quantize_batch": [vp, i32, vp],
                 "fp8_quantize_f32": [vp, i64, i32, vp, vp, vp, vp],
                 "fp8_set_bias": [i32, vp, vp, vp, vp],
                 "fp8_cast_stats": [vp, i64, i64, i64, i32, vp, i32, vp, vp, vp],
@@ -190,6 +192,35 @@ def fp8_quantize(x: torch.Tensor, fmt: int, gran: int, margin: int = 0, scale: P
     rows, cols, ld = _matrix(x)
     _check("fp8_quantize", lib().fp8_quantize(_p(x), rows, cols, ld, fmt, gran, margin, _p(scale), _p(q_row),
                                               _p(q_col), _p(sf_row), _p(sf_col), _p(amax), _stream(stream)))
+
+
+class QuantizeDesc(ctypes.Structure):
+    """One cast of fp8_quantize_batch (fp8_quantize_desc in fp8q.h)."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("ld", ctypes.c_int64),
+                ("fmt", ctypes.c_int32), ("gran", ctypes.c_int32), ("margin", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("scale", ctypes.c_void_p), ("q_row", ctypes.c_void_p),
+                ("q_col", ctypes.c_void_p), ("sf_row", ctypes.c_void_p), ("sf_col", ctypes.c_void_p),
+                ("amax", ctypes.c_void_p)]
+
+
+QUANTIZE_BATCH_MAX = 4  # FP8_QUANTIZE_BATCH_MAX
+
+
+def fp8_quantize_batch(casts, stream=None) -> None:
+    """Up to QUANTIZE_BATCH_MAX fp8_quantize casts in one launch.  Each cast is a dict with the keyword
+    arguments of fp8_quantize: x, fmt, gran and optionally margin, scale, q_row, q_col, sf_row, sf_col,
+    amax (see fp8_quantize_batch in fp8q.h)."""
+    casts = list(casts)
+    descs = (QuantizeDesc * max(len(casts), 1))()
+    for d, c in zip(descs, casts):
+        d.rows, d.cols, d.ld = _matrix(c["x"])
+        d.x = _p(c["x"])
+        d.fmt, d.gran, d.margin, d.reserved = int(c["fmt"]), int(c["gran"]), int(c.get("margin", 0)), 0
+        d.scale, d.amax = _p(c.get("scale")), _p(c.get("amax"))
+        d.q_row, d.q_col = _p(c.get("q_row")), _p(c.get("q_col"))
+        d.sf_row, d.sf_col = _p(c.get("sf_row")), _p(c.get("sf_col"))
+    _check("fp8_quantize_batch", lib().fp8_quantize_batch(ctypes.cast(descs, ctypes.c_void_p), len(casts),
+                                                          _stream(stream)))
 
 
 def fp8_quantize_f32(x: torch.Tensor, fmt: int, q: torch.Tensor, scale: Ptr = None, amax: Ptr = None,

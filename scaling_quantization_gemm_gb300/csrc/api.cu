@@ -37,6 +37,7 @@ fp8_status launch_quantize_f32(const float* x, int64_t n, int fmt, const float* 
                                cudaStream_t st);
 fp8_status launch_cast_stats(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, const float* scales,
                              int n, uint64_t* saturated, uint64_t* underflow, cudaStream_t st);
+fp8_status launch_quantize_batch(const fp8_quantize_desc* descs, int n, cudaStream_t st);
 fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int gran, int margin,
                            const float* scale, uint8_t* q_row, uint8_t* q_col, void* sf_row, void* sf_col,
                            float* amax, cudaStream_t st);
@@ -151,10 +152,15 @@ fp8_status fp8_amax_history_update_batch(const fp8_history_state* states, int32_
     return launch_history_batch(states, n, as_stream(stream));
 }
 
-fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, fp8_format fmt, fp8_granularity gran,
-                        int32_t margin, const float* scale, uint8_t* q_row, uint8_t* q_col, void* sf_row,
-                        void* sf_col, float* amax, void* stream) {
-    g_detail[0] = 0;
+}  // extern "C"
+
+namespace fp8q {
+namespace {
+
+// The checks of one fp8_quantize call (shared with fp8_quantize_batch).
+fp8_status check_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int gran,
+                          const float* scale, const uint8_t* q_row, const uint8_t* q_col, const void* sf_row,
+                          const void* sf_col, const float* amax) {
     fp8_status s = check_bf16_matrix(x, rows, cols, ld);
     if (s != FP8_OK) return s;
     s = check_tma_dims(rows, cols);
@@ -183,8 +189,43 @@ fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, f
                     (long long)rows);
         FP8_REQUIRE(aligned(q_col, 16), FP8_ERR_UNSUPPORTED, "q_col must be 16-byte aligned");
     }
+    return FP8_OK;
+}
+
+}  // namespace
+}  // namespace fp8q
+
+extern "C" {
+
+fp8_status fp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, fp8_format fmt, fp8_granularity gran,
+                        int32_t margin, const float* scale, uint8_t* q_row, uint8_t* q_col, void* sf_row,
+                        void* sf_col, float* amax, void* stream) {
+    g_detail[0] = 0;
+    fp8_status s = check_quantize(x, rows, cols, ld, fmt, gran, scale, q_row, q_col, sf_row, sf_col, amax);
+    if (s != FP8_OK || rows == 0 || cols == 0) return s;
     return launch_quantize(x, rows, cols, ld, fmt, gran, margin, scale, q_row, q_col, sf_row, sf_col, amax,
                            as_stream(stream));
+}
+
+fp8_status fp8_quantize_batch(const fp8_quantize_desc* descs, int32_t n, void* stream) {
+    g_detail[0] = 0;
+    FP8_REQUIRE(n >= 0 && n <= FP8_QUANTIZE_BATCH_MAX, FP8_ERR_INVALID_ARG, "n = %d outside [0, %d]", (int)n,
+                FP8_QUANTIZE_BATCH_MAX);
+    if (n == 0) return FP8_OK;
+    FP8_REQUIRE(descs != nullptr, FP8_ERR_INVALID_ARG, "descs is NULL");
+    for (int i = 0; i < n; ++i) {
+        const fp8_quantize_desc& d = descs[i];
+        FP8_REQUIRE(d.reserved == 0, FP8_ERR_INVALID_ARG, "descriptor %d: reserved must be 0", i);
+        fp8_status s = check_quantize(d.x, d.rows, d.cols, d.ld, d.fmt, d.gran, d.scale, d.q_row, d.q_col, d.sf_row,
+                                      d.sf_col, d.amax);
+        if (s != FP8_OK) {
+            char why[sizeof g_detail];
+            snprintf(why, sizeof why, "%s", g_detail);
+            set_error_detail("descriptor %d: %s", i, why);
+            return s;
+        }
+    }
+    return launch_quantize_batch(descs, n, as_stream(stream));
 }
 
 fp8_status fp8_quantize_current(const void* x, int64_t rows, int64_t cols, int64_t ld, fp8_format fmt, int32_t margin,

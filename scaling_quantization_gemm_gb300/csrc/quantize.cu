@@ -36,6 +36,7 @@ namespace {
 constexpr int kTile = 128;     // tile is kTile x kTile bf16 elements (32 KB)
 constexpr int kThreads = 256;
 constexpr int kQStages = 2;    // TMA ring depth (3 CTAs per SM)
+constexpr uint32_t kHalfBytes = kTile * 64 * 2;  // a tile is loaded as two 64-column halves (16 KB each)
 
 struct QuantArgs {
     int64_t rows, cols;
@@ -200,23 +201,37 @@ __device__ __forceinline__ void stage_col32(uint32_t base, int c, int seg, const
 // arrival).  Row-wise only, warps never wait for one another except where a
 // tile needs a cross-warp reduction (128x128 blocks); with the column-wise copy
 // the CTA works in lock step (the codes are staged in the stage all warps read).
-// Row pass: thread t holds the 16-byte chunk column j = t % 16 of
-// rows t/16 + 16 i, i = 0..7.  Column pass: warp w covers column pairs
-// lane + 32 (w & 1) over the 32-row segment w / 2.
+// A tile arrives as two 64-column halves (two TMA loads), each 128 rows of 128
+// bytes in the 128-byte swizzle: 16-byte chunk k of row r is stored at chunk
+// k ^ (r % 8).  Row pass: each thread casts 16 columns of four rows 32 apart
+// (the mapping is spelled out below); a warp instruction covers four whole
+// rows.  Column pass: warp w covers column pairs lane + 32 (w & 1) over the
+// 32-row segment w / 2.  Both passes' shared-memory reads are free of bank
+// conflicts.
 // The tile loop (shared by the cast kernel and the fused current-scaling kernel).  For
 // per-tensor scaling `s_given` is the scale; block granularities compute their own.  With
 // `from_end` the CTAs walk the tiles from the last one back (the fused kernel's amax pass reads x
 // front to back, so the tiles it read last are the likeliest to be still in L2).
 template <int GRAN, int FMT>
-__device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const QuantArgs& a, float s_given,
-                                               bool from_end = false) {
+__device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const QuantArgs& a, float s_given, int cta,
+                                               int ctas, bool from_end = false) {
     const CUtensorMap* tmX = &maps->x;
     extern __shared__ uint8_t smem_raw[];
     QuantSmem& S = *reinterpret_cast<QuantSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int j = tid & 15;
-    const int rsub = tid >> 4;
-    const int64_t n_my = (a.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    // Row pass: in visit v (0..3) the thread casts 16 columns (two 16-byte chunks) of tile row
+    // 32 v + rl: half h = bit 3 of the lane, chunk pair cp = lane % 4 of that half, rl = 4 warp +
+    // 2 (lane / 16) + (lane / 4) % 2.  A warp instruction covers 4 whole rows (128 bytes each: full
+    // lines for the row-wise stores); the 8 lanes of a quarter warp read one half of two adjacent rows,
+    // whose swizzled chunks fall in 8 different bank groups.  A 1x32 block is two neighbouring lanes
+    // (lane ^ 1), a 1x128 row block the 8 lanes that differ in bits 0, 1 and 3.
+    const int rh = (lane >> 3) & 1, rcp = lane & 3;
+    const int rl = 4 * warp + 2 * (lane >> 4) + ((lane >> 2) & 1);
+    uint32_t row_off[2];  // byte offsets of the thread's two chunks within row rl of its half
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+        row_off[c] = (uint32_t)rh * kHalfBytes + (uint32_t)rl * 128u + ((uint32_t)((2 * rcp + c) ^ (rl & 7)) << 4);
+    const int64_t n_my = (a.ntiles - cta + ctas - 1) / ctas;
 
     // tiles that need a block-wide reduction, and the staged column-wise copy, keep the CTA in lock step
     constexpr bool kMX = GRAN == FP8_SCALE_MX_1x32 || GRAN == FP8_SCALE_MX_1x32_OCP;
@@ -234,15 +249,42 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
     // outputs (measured: row+col per-tensor cast 6 % faster); the block granularities measured
     // slower with the hint and load without it.
     const uint64_t policy = GRAN == FP8_SCALE_TENSOR && tid == 0 ? l2_policy_evict_first() : 0;
-    auto issue = [&](int64_t i) {  // TMA load of this CTA's i-th tile into stage i % kQStages
-        const int64_t tile = from_end ? a.ntiles - 1 - (blockIdx.x + i * gridDim.x) : blockIdx.x + i * gridDim.x;
+    // Tile coordinates (tile row, tile column) advance by the grid size each step, with a carry: one
+    // division per CTA instead of a 64-bit division per tile in every thread.
+    const int tiles_c = (int)a.tiles_c;
+    const int step_r = (int)(ctas / a.tiles_c), step_c = (int)(ctas % a.tiles_c);
+    const int64_t first = from_end ? a.ntiles - 1 - cta : cta;
+    auto advance = [&](int& tr, int& tc) {
+        if (from_end) {
+            tr -= step_r;
+            tc -= step_c;
+            if (tc < 0) {
+                tc += tiles_c;
+                --tr;
+            }
+        } else {
+            tr += step_r;
+            tc += step_c;
+            if (tc >= tiles_c) {
+                tc -= tiles_c;
+                ++tr;
+            }
+        }
+    };
+    int ld_tr = (int)(first / a.tiles_c), ld_tc = (int)(first % a.tiles_c);  // next tile to load (thread 0)
+    auto issue = [&](int64_t i) {  // TMA load of this CTA's i-th tile (the next one in order) into stage i % kQStages
         const int st = (int)(i % kQStages);
-        const int x0 = (int)((tile % a.tiles_c) * kTile), y0 = (int)((tile / a.tiles_c) * kTile);
+        const int x0 = ld_tc * kTile, y0 = ld_tr * kTile;
+        advance(ld_tr, ld_tc);
         mbar_arrive_expect_tx(smem_u32(&S.full[st]), kTile * kTile * 2);
-        if constexpr (GRAN == FP8_SCALE_TENSOR)
-            tma_load_2d_hint(smem_u32(S.tile[st]), tmX, smem_u32(&S.full[st]), x0, y0, policy);
-        else
-            tma_load_2d(smem_u32(S.tile[st]), tmX, smem_u32(&S.full[st]), x0, y0);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // two 64-column halves, 128-byte rows in the 128B swizzle
+            if constexpr (GRAN == FP8_SCALE_TENSOR)
+                tma_load_2d_hint(smem_u32(S.tile[st]) + h * kHalfBytes, tmX, smem_u32(&S.full[st]), x0 + 64 * h, y0,
+                                 policy);
+            else
+                tma_load_2d(smem_u32(S.tile[st]) + h * kHalfBytes, tmX, smem_u32(&S.full[st]), x0 + 64 * h, y0);
+        }
     };
     int64_t issued = 0;  // meaningful in thread 0
     if (tid == 0) {
@@ -262,8 +304,9 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
         s2_tensor = sb | (sb << 16);
     }
     uint32_t amax_acc = 0;
+    int cur_tr = (int)(first / a.tiles_c), cur_tc = (int)(first % a.tiles_c);  // tile being cast
 
-    for (int64_t i = 0; i < n_my; ++i) {
+    for (int64_t i = 0; i < n_my; ++i, advance(cur_tr, cur_tc)) {
         if (tid == 0 && i >= 1 && i + 1 < n_my) {
             // stage (i+1) % 2 held tile i-1: wait until every warp has released it and the TMA store
             // of its column-wise codes has read it, then refill
@@ -282,28 +325,30 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
         } else if (!ok) {
             break;
         }
-        const uint16_t* T = S.tile[st];
-        const int64_t tile = from_end ? a.ntiles - 1 - (blockIdx.x + i * gridDim.x) : blockIdx.x + i * gridDim.x;
-        const int64_t r0 = (tile / a.tiles_c) * kTile, c0 = (tile % a.tiles_c) * kTile;
-        const int64_t col = c0 + 8 * j;
-        const bool col_ok = col < a.cols;
+        const uint32_t Tb = smem_u32(S.tile[st]);
+        const int64_t r0 = (int64_t)cur_tr * kTile, c0 = (int64_t)cur_tc * kTile;
         const int parity = (int)(i & 1);
 
-        uint4 v[8];
-        uint32_t cm[8];  // |x| max of each chunk, bf16 bits
+        // row pass, loads: visit v reads row 32 v + rl (rows 32 apart keep the swizzle phase: rl % 8)
+        uint4 v[4][2];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            v[k] = *reinterpret_cast<const uint4*>(&T[(rsub + 16 * k) * kTile + 8 * j]);
-            cm[k] = absmax_fold(absmax_acc(absmax_acc(absmax_acc(v[k].x, v[k].y), v[k].z), v[k].w));
-            amax_acc = max(amax_acc, cm[k]);
+        for (int vi = 0; vi < 4; ++vi)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) v[vi][c] = ld_shared_v4(Tb + (uint32_t)(32 * vi) * 128u + row_off[c]);
+        uint32_t pm[4] = {0, 0, 0, 0};  // |x| max of the thread's 16 columns in each visit, bf16 bits
+        if (GRAN != FP8_SCALE_TENSOR || a.amax != nullptr) {
+#pragma unroll
+            for (int vi = 0; vi < 4; ++vi) {
+                const uint4 x0 = v[vi][0], x1 = v[vi][1];
+                pm[vi] = absmax_fold(absmax_acc(absmax_acc(absmax_acc(x0.x, x0.y), absmax_acc(x0.z, x0.w)),
+                                                absmax_acc(absmax_acc(x1.x, x1.y), absmax_acc(x1.z, x1.w))));
+                amax_acc = max(amax_acc, pm[vi]);
+            }
         }
 
         int e_tile = 0;
         if constexpr (GRAN == FP8_SCALE_BLOCK_128x128) {
-            uint32_t m = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) m = max(m, cm[k]);
-            m = __reduce_max_sync(0xffffffffu, m);
+            uint32_t m = __reduce_max_sync(0xffffffffu, max(max(pm[0], pm[1]), max(pm[2], pm[3])));
             if (lane == 0) S.red[parity][warp] = m;
             __syncthreads();
             m = S.red[parity][0];
@@ -319,41 +364,47 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
 
         // ---------------------------------------------------------- row-wise
         if (a.do_row) {
+            const int64_t cc = c0 + 64 * rh + 16 * rcp;  // the thread's first column
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int64_t r = r0 + rsub + 16 * k;
-                const bool okr = col_ok && r < a.rows;
+            for (int vi = 0; vi < 4; ++vi) {
+                const int64_t r = r0 + 32 * vi + rl;
+                const bool row_ok = r < a.rows;
                 uint32_t s2;
                 if constexpr (GRAN == FP8_SCALE_TENSOR) {
                     s2 = s2_tensor;
                 } else if constexpr (GRAN == FP8_SCALE_BLOCK_128x128) {
                     s2 = pow2_bf16x2(e_tile);
                 } else if constexpr (kMX) {
-                    uint32_t m = cm[k];
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                    const uint32_t m = max(pm[vi], __shfl_xor_sync(0xffffffffu, pm[vi], 1));
                     const int e = block_bias<GRAN>(m, FMT, a.margin);
                     s2 = pow2_bf16x2(e);
-                    if ((j & 3) == 0 && okr)
-                        static_cast<uint8_t*>(a.sf_row)[r * cdiv(a.cols, 32) + (col >> 5)] = (uint8_t)(127 - e);
+                    if ((rcp & 1) == 0 && row_ok && cc < a.cols)
+                        static_cast<uint8_t*>(a.sf_row)[r * cdiv(a.cols, 32) + (cc >> 5)] = (uint8_t)(127 - e);
                 } else {  // 1x128
-                    uint32_t m = cm[k];
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                    uint32_t m = max(pm[vi], __shfl_xor_sync(0xffffffffu, pm[vi], 1));
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
                     const int e = bias_bf16(m, FMT, a.margin);
                     s2 = pow2_bf16x2(e);
-                    if (j == 0 && r < a.rows)
+                    if (rh == 0 && rcp == 0 && row_ok)
                         static_cast<float*>(a.sf_row)[r * cdiv(a.cols, kTile) + c0 / kTile] = pow2_exact(-e);
                 }
-                if (okr) {
-                    uint2 c;
-                    if (GRAN != FP8_SCALE_TENSOR || pow2_tensor)
-                        c = encode8<FMT>(v[k], s2);
-                    else
-                        c = encode8_f32<FMT>(v[k], s_tensor);
-                    *reinterpret_cast<uint2*>(a.q_row + r * a.cols + col) = c;
+                if (row_ok) {
+                    uint2 q0, q1;
+                    if (GRAN != FP8_SCALE_TENSOR || pow2_tensor) {
+                        q0 = encode8<FMT>(v[vi][0], s2);
+                        q1 = encode8<FMT>(v[vi][1], s2);
+                    } else {
+                        q0 = encode8_f32<FMT>(v[vi][0], s_tensor);
+                        q1 = encode8_f32<FMT>(v[vi][1], s_tensor);
+                    }
+                    uint8_t* dst = a.q_row + r * a.cols + cc;
+                    if (cc + 16 <= a.cols && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(q0.x, q0.y, q1.x, q1.y);
+                    } else {
+                        if (cc < a.cols) *reinterpret_cast<uint2*>(dst) = q0;
+                        if (cc + 8 < a.cols) *reinterpret_cast<uint2*>(dst + 8) = q1;
+                    }
                 }
             }
         }
@@ -362,9 +413,13 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
         if (a.do_col) {
             const int cp = lane + 32 * (warp & 1);  // column pair within the tile
             const int seg = warp >> 1;              // 32-row segment within the tile
+            // word (rows 32 seg + rr, columns 2 cp, 2 cp + 1): half cp / 32, 16-byte chunk (cp % 32) / 4 of the
+            // row's 128 bytes, stored at chunk ((cp % 32) / 4) ^ (row % 8); row % 8 = rr % 8
+            const uint32_t cbase = Tb + (uint32_t)(warp & 1) * kHalfBytes + (uint32_t)(32 * seg) * 128u + 4u * (lane & 3);
             uint32_t w[32];
 #pragma unroll
-            for (int r = 0; r < 32; ++r) w[r] = *reinterpret_cast<const uint32_t*>(&T[(32 * seg + r) * kTile + 2 * cp]);
+            for (int rr = 0; rr < 32; ++rr)
+                w[rr] = ld_shared_u32(cbase + (uint32_t)rr * 128u + ((uint32_t)((lane >> 2) ^ (rr & 7)) << 4));
             uint32_t mm = w[0];
 #pragma unroll
             for (int r = 1; r < 32; ++r) mm = absmax_acc(mm, w[r]);
@@ -425,12 +480,12 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
             // above already says so): the codes go into its stage and leave as one TMA store, which clips
             // the rows and columns past the tensor's edge
             if constexpr (!(kMX || GRAN == FP8_SCALE_BLOCK_1x128)) __syncthreads();
-            stage_col32(smem_u32(T), 2 * cp, seg, o);
-            stage_col32(smem_u32(T), 2 * cp + 1, seg, oB);
+            stage_col32(Tb, 2 * cp, seg, o);
+            stage_col32(Tb, 2 * cp + 1, seg, oB);
             fence_proxy_async_smem();
             __syncthreads();
             if (tid == 0) {
-                tma_store_2d(&maps->qc, smem_u32(T), (int)r0, (int)c0);
+                tma_store_2d(&maps->qc, Tb, (int)r0, (int)c0);
                 bulk_commit();
             }
         }
@@ -466,9 +521,58 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
     }
 }
 
+template <int GRAN>
+__device__ __forceinline__ float tensor_scale(const QuantArgs& a) {
+    if constexpr (GRAN == FP8_SCALE_TENSOR)
+        return *a.scale;
+    else
+        return 1.0f;
+}
+
 template <int GRAN, int FMT>
 __global__ void __launch_bounds__(kThreads, 3) quantize_tile_kernel(const __grid_constant__ QuantMaps maps, QuantArgs a) {
-    quantize_tiles<GRAN, FMT>(&maps, a, GRAN == FP8_SCALE_TENSOR ? *a.scale : 1.0f);
+    quantize_tiles<GRAN, FMT>(&maps, a, tensor_scale<GRAN>(a), blockIdx.x, gridDim.x);
+}
+
+// ----------------------------------------------------------- batched casts
+//
+// Several casts in one launch (fp8_quantize_batch): the grid is split among the tensors in
+// proportion to their tiles, and each CTA runs the tile loop of one tensor with its own granularity
+// and format, as a CTA of that tensor's own launch would, over its share of the grid.  The batch
+// pays one launch, one fill and one tail instead of one per tensor.
+constexpr int kMaxBatch = FP8_QUANTIZE_BATCH_MAX;
+
+struct QuantBatch {
+    QuantMaps maps[kMaxBatch];
+    QuantArgs a[kMaxBatch];
+    int cta0[kMaxBatch + 1];  // tensor k's CTAs are cta0[k] .. cta0[k + 1] - 1
+    int kind[kMaxBatch];      // granularity * 2 + format
+    int n;
+};
+
+__global__ void __launch_bounds__(kThreads, 3) quantize_batch_kernel(const __grid_constant__ QuantBatch b) {
+    int k = 0;
+    while (k + 1 < b.n && (int)blockIdx.x >= b.cta0[k + 1]) ++k;
+    const int cta = (int)blockIdx.x - b.cta0[k], ctas = b.cta0[k + 1] - b.cta0[k];
+    const QuantMaps* m = &b.maps[k];
+    const QuantArgs& a = b.a[k];
+    switch (b.kind[k]) {
+#define FP8Q_BATCH_CASE(G)                                                                    \
+    case 2 * (G) + FP8_E4M3:                                                                  \
+        quantize_tiles<G, FP8_E4M3>(m, a, tensor_scale<G>(a), cta, ctas);                    \
+        break;                                                                                \
+    case 2 * (G) + FP8_E5M2:                                                                  \
+        quantize_tiles<G, FP8_E5M2>(m, a, tensor_scale<G>(a), cta, ctas);                    \
+        break;
+        FP8Q_BATCH_CASE(FP8_SCALE_TENSOR)
+        FP8Q_BATCH_CASE(FP8_SCALE_BLOCK_1x128)
+        FP8Q_BATCH_CASE(FP8_SCALE_BLOCK_128x128)
+        FP8Q_BATCH_CASE(FP8_SCALE_MX_1x32)
+        FP8Q_BATCH_CASE(FP8_SCALE_MX_1x32_OCP)
+#undef FP8Q_BATCH_CASE
+        default:
+            break;
+    }
 }
 
 // ------------------------------------------------- fused current scaling
@@ -574,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (s_abort) return;
 
     // phase 2: the cast
-    quantize_tiles<FP8_SCALE_TENSOR, FMT>(&maps, a, s_scale, /*from_end=*/true);
+    quantize_tiles<FP8_SCALE_TENSOR, FMT>(&maps, a, s_scale, blockIdx.x, gridDim.x, /*from_end=*/true);
 }
 
 // Per-tensor scaled cast of an fp32 tensor: q = Encode(fl32(x s)), grid-stride over 8-element
@@ -856,10 +960,10 @@ fp8_status make_x_map(const void* x, int64_t rows, int64_t cols, int64_t ld, CUt
     FP8_REQUIRE(fn != nullptr, FP8_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kTile, (cuuint32_t)kTile};
+    cuuint32_t box[2] = {64, (cuuint32_t)kTile};  // one 64-column half of a tile: 128-byte rows
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     FP8_REQUIRE(r == CUDA_SUCCESS, FP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return FP8_OK;
@@ -963,6 +1067,54 @@ fp8_status launch_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld
     return FP8_ERR_UNSUPPORTED;
 }
 
+fp8_status launch_quantize_batch(const fp8_quantize_desc* descs, int n, cudaStream_t st) {
+    QuantBatch b;
+    memset(&b, 0, sizeof b);
+    int64_t tiles[kMaxBatch];
+    int m = 0;  // non-empty casts
+    for (int i = 0; i < n; ++i) {
+        const fp8_quantize_desc& d = descs[i];
+        if (d.rows == 0 || d.cols == 0) continue;
+        fp8_status s = make_maps(d.x, d.rows, d.cols, d.ld, d.q_col, &b.maps[m]);
+        if (s != FP8_OK) return s;
+        b.a[m] = quant_args(d.rows, d.cols, d.margin, d.scale, d.q_row, d.q_col, d.sf_row, d.sf_col, d.amax);
+        b.kind[m] = 2 * d.gran + d.fmt;
+        tiles[m] = b.a[m].ntiles;
+        ++m;
+    }
+    if (m == 0) return FP8_OK;
+    b.n = m;
+    const size_t smem = sizeof(QuantSmem) + 1024;
+    int occ = 0;
+    fp8_status s = resident_ctas(reinterpret_cast<const void*>(quantize_batch_kernel), kThreads, smem, &occ);
+    if (s != FP8_OK) return s;
+    int64_t total = 0;
+    for (int k = 0; k < m; ++k) total += tiles[k];
+    const int64_t cap = (int64_t)device_sm_count() * occ;
+    const int grid = (int)(total < cap ? total : cap);  // >= m: every tensor has a tile
+    // one CTA per tensor, then each further CTA to the tensor whose share has the most rounds of tiles
+    // left: the launch lasts as long as its slowest share
+    int share[kMaxBatch];
+    for (int k = 0; k < m; ++k) share[k] = 1;
+    for (int used = m; used < grid; ++used) {
+        int best = -1;
+        int64_t best_rounds = 0;
+        for (int k = 0; k < m; ++k) {
+            const int64_t rounds = (tiles[k] + share[k] - 1) / share[k];
+            if (share[k] < tiles[k] && rounds > best_rounds) {
+                best = k;
+                best_rounds = rounds;
+            }
+        }
+        if (best < 0) break;
+        ++share[best];
+    }
+    b.cta0[0] = 0;
+    for (int k = 0; k < m; ++k) b.cta0[k + 1] = b.cta0[k] + share[k];
+    quantize_batch_kernel<<<b.cta0[m], kThreads, smem, st>>>(b);
+    return check_launch("batched quantize kernel launch");
+}
+
 fp8_status launch_quantize_current(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, int margin,
                                    uint8_t* q_row, uint8_t* q_col, float* amax, int32_t* bias, float* scale,
                                    float* scale_inv, void* workspace, int32_t* status, cudaStream_t st) {
@@ -992,13 +1144,14 @@ fp8_status launch_quantize_current(const void* x, int64_t rows, int64_t cols, in
 //
 // The array is kNoAllocScratchBytes (4 KB) on every GPU that loads the library,
 // held until the process exits: a 16-byte header (arrival count, generation,
-// scale) and one 4-byte partial per CTA, so at most (4096 - 16) / 4 = 1020 CTAs.
-// A launch that would need more is rejected.  Every call shares the array and
+// scale) and one 4-byte partial per CTA, so at most (4096 - 16) / 4 = 1020 CTAs;
+// the grid is capped there (GB300 runs 456).  Every call shares the array and
 // finds the previous call's contents there; the call clears the header on its
 // stream before the kernel, and each CTA writes its partial before any CTA reads
 // it.  Calls whose kernels overlap on the GPU (other streams, other host threads)
 // race on the array.
 constexpr int kNoAllocScratchBytes = 4096;
+constexpr int kNoAllocMaxCtas = (kNoAllocScratchBytes - kCurrentWsHeader) / 4;
 static __device__ __align__(256) unsigned char g_current_scratch[kNoAllocScratchBytes];
 
 namespace {
@@ -1011,17 +1164,21 @@ fp8_status noalloc_scratch(void** out) {
     cudaError_t e = cudaGetDevice(&dev);
     FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     FP8_REQUIRE(dev >= 0 && dev < 64, FP8_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+    // read without a lock once cached; the mutex only serialises the first lookup on a device
+    static std::atomic<void*> addr[64];
     static std::mutex mu;
-    static void* addr[64] = {nullptr};
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_current_scratch);
-        FP8_REQUIRE(e == cudaSuccess && p != nullptr, FP8_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s",
-                    cudaGetErrorString(e));
-        addr[dev] = p;
+    void* p = addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        std::lock_guard<std::mutex> lock(mu);
+        p = addr[dev].load(std::memory_order_relaxed);
+        if (p == nullptr) {
+            e = cudaGetSymbolAddress(&p, g_current_scratch);
+            FP8_REQUIRE(e == cudaSuccess && p != nullptr, FP8_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s",
+                        cudaGetErrorString(e));
+            addr[dev].store(p, std::memory_order_release);
+        }
     }
-    *out = addr[dev];
+    *out = p;
     return FP8_OK;
 }
 
@@ -1035,6 +1192,8 @@ fp8_status launch_current_noalloc(const QuantMaps& tm, const QuantArgs& a, const
     if (s != FP8_OK) return s;
     int64_t grid = (int64_t)device_sm_count() * occ;  // all CTAs resident at once (grid barrier)
     if (grid > a.ntiles) grid = a.ntiles;
+    // one scratch slot per CTA: fewer CTAs than fit only lengthen each CTA's grid-stride loops
+    if (grid > kNoAllocMaxCtas) grid = kNoAllocMaxCtas;
     if (grid < 1) grid = 1;
     const int64_t need = kCurrentWsHeader + 4 * grid;
     FP8_REQUIRE(need <= kNoAllocScratchBytes, FP8_ERR_UNSUPPORTED,

@@ -38,9 +38,8 @@ import torch
 
 from . import (BLOCK_1x128, BLOCK_128x128, DGRAD, E4M3, E5M2, FPROP, MX_1x32, MX_1x32_OCP, TENSOR, WGRAD,
                current_workspace, fp8_amax, fp8_amax_history_update, fp8_amax_history_update_batch, fp8_cast_stats,
-               fp8_compute_scale,
-               fp8_compute_scale_ratio, fp8_quantize, fp8_quantize_current, fp8_scaled_gemm, fp8_scaled_gemm_quantize,
-               fp8_set_bias)
+               fp8_compute_scale, fp8_compute_scale_ratio, fp8_quantize, fp8_quantize_batch, fp8_quantize_current,
+               fp8_scaled_gemm, fp8_scaled_gemm_quantize, fp8_set_bias)
 
 
 class ScaleState:
@@ -177,8 +176,18 @@ class LinearFwdBwd:
             fp8_quantize(x, st.fmt, TENSOR, scale=st.scale, q_row=qr, q_col=qc, amax=st.amax)
 
     def quantize(self) -> None:
-        for i in range(3):
-            self.quantize_one(i)
+        """The three casts.  Once every history holds a scale (or with the fixed first step), they are
+        one batched launch: each cast uses its delayed scale and records its amax."""
+        states = (self.sx, self.sw, self.sg)
+        if self.first_step == "fixed" or all(st.steps > 0 for st in states):
+            fp8_quantize_batch(
+                dict(x=x, fmt=st.fmt, gran=TENSOR, scale=st.scale, q_row=qr, q_col=qc, amax=st.amax)
+                for x, st, qr, qc in ((self.X, self.sx, self.qx_row, self.qx_col),
+                                      (self.W, self.sw, self.qw_row, self.qw_col),
+                                      (self.dY, self.sg, self.qg_row, self.qg_col)))
+        else:
+            for i in range(3):
+                self.quantize_one(i)
 
     def gemms(self) -> None:
         fp8_scaled_gemm(FPROP, self.qx_row, E4M3, TENSOR, self.sx.scale_inv, self.qw_row, E4M3, TENSOR,
@@ -243,10 +252,12 @@ class BlockLinearFwd:
             sbytes(N, K, self.gw) + (sbytes(K, M, self.gx) + sbytes(K, N, self.gw) if col else 0)
 
     def quantize(self) -> None:
-        fp8_quantize(self.X, E4M3, self.gx, self.margin, q_row=self.qx_row, q_col=self.qx_col, sf_row=self.sx_row,
-                     sf_col=self.sx_col)
-        fp8_quantize(self.W, E4M3, self.gw, self.margin, q_row=self.qw_row, q_col=self.qw_col, sf_row=self.sw_row,
-                     sf_col=self.sw_col)
+        """Both casts in one batched launch."""
+        fp8_quantize_batch([
+            dict(x=self.X, fmt=E4M3, gran=self.gx, margin=self.margin, q_row=self.qx_row, q_col=self.qx_col,
+                 sf_row=self.sx_row, sf_col=self.sx_col),
+            dict(x=self.W, fmt=E4M3, gran=self.gw, margin=self.margin, q_row=self.qw_row, q_col=self.qw_col,
+                 sf_row=self.sw_row, sf_col=self.sw_col)])
 
     def gemm(self) -> None:
         fp8_scaled_gemm(FPROP, self.qx_row, E4M3, self.gx, self.sx_row, self.qw_row, E4M3, self.gw, self.sw_row,

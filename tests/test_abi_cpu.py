@@ -116,6 +116,36 @@ def test_gemm_validation(L):
     assert g(*args(M=0)) == 0  # empty output: no-op
 
 
+def test_quantize_batch_validation(L):
+    """fp8_quantize_batch: the descriptor layout (96 bytes), n in [0, 4], reserved = 0, and every
+    descriptor checked as fp8_quantize checks its arguments before anything is launched; the error
+    detail names the descriptor."""
+    import scaling_quantization_gemm_gb300 as q
+    assert ctypes.sizeof(q.QuantizeDesc) == 96 and q.QUANTIZE_BATCH_MAX == 4
+    text = open(HEADER).read()
+    assert re.search(r"#define FP8_QUANTIZE_BATCH_MAX (\d+)", text).group(1) == "4"
+    f = L.fp8_quantize_batch
+    assert f(None, 0, None) == 0  # empty: no-op
+    assert f(None, -1, None) == 1 and f(None, 5, None) == 1
+    assert f(None, 2, None) == 1  # NULL descriptors
+    descs = (q.QuantizeDesc * 3)()
+    for d in descs:
+        d.x, d.rows, d.cols, d.ld, d.fmt, d.gran = FAKE, 32, 64, 64, 0, 3
+        d.q_row, d.sf_row = FAKE, FAKE
+    descs[0].gran, descs[0].sf_row, descs[0].scale = 0, None, FAKE  # per-tensor
+    addr = ctypes.cast(descs, ctypes.c_void_p)
+    # descriptor 2 invalid in turn: rejected before any launch, detail names it
+    for field, bad, good, code in (("reserved", 1, 0, 1), ("fmt", 4, 0, 1), ("gran", 9, 3, 1), ("ld", 32, 64, 1),
+                                   ("cols", 60, 64, 2), ("x", FAKE + 8, FAKE, 2), ("sf_row", None, FAKE, 1),
+                                   ("q_row", FAKE + 4, FAKE, 2), ("rows", -1, 32, 1)):
+        setattr(descs[2], field, bad)
+        assert f(addr, 3, None) == code, field
+        assert _detail(L).startswith("descriptor 2:"), (field, _detail(L))
+        setattr(descs[2], field, good)
+    descs[1].scale = FAKE  # a block cast given a per-tensor scale
+    assert f(addr, 3, None) == 1 and _detail(L).startswith("descriptor 1:")
+
+
 def test_block_scaled_k_rule_matches_the_header(L):
     """The header states that every block-scaled mode needs K % 128 == 0; the check returns
     FP8_ERR_UNSUPPORTED for K = 32, 64, 96 and 160 in each mode (MX 1x32 included)."""
