@@ -15,8 +15,7 @@
 //               (fp32, bf16, or E4M3/E5M2 with a given scale and a fused amax),
 //               store.  Each warp owns the 32 TMEM lanes (= tile rows) that its
 //               warp index selects.
-//   warps 6-9   (block-scaled kernels only) scale-factor writers; warp 10 (CTA-pair
-//               block-scaled kernel) re-encodes fp32 block scales for them.
+//   warps 6-9   (block-scaled kernels only) scale-factor writers.
 // Two fp32 accumulators live in TMEM so the epilogue of one tile overlaps the
 // main loop of the next.  M > 128 runs on CTA pairs (clusters of two, tcgen05
 // cta_group::2: the even CTA issues the MMAs for both SMs); M <= 128 runs the
@@ -754,13 +753,12 @@ __global__ void __launch_bounds__(320, 1)
 // B row n: lane 32q + n%32, column 8 + n/32, every quarter q).  The producer
 // TMA-loads the scales of each group of four K tiles (16 bytes per row: the A
 // rows of this CTA and all B rows of the tile) into a four-slot shared-memory
-// ring, two groups ahead.  fp32 block scales (1x128, 128x128: powers of two)
-// are rewritten in their slot by a converter warp as E8M0 words in the MX
-// layout, repeated over the four 32-wide sub-blocks of a K tile and, for
-// 128x128 blocks, over the rows of a block.  When a group's words are ready,
-// each writer thread reads those of its rows for the group's four K tiles into
-// registers and frees the slot, so what a writer does after waiting for a TMEM
-// slot is the same few stores for every scale kind.  TMEM has room for four
+// ring, two groups ahead.  When a group lands, each writer thread reads the
+// words of its rows for the group's four K tiles into registers -- E8M0 words
+// as they are; power-of-two fp32 block scales (1x128, 128x128) re-encoded as
+// E8M0 and repeated over the four 32-wide sub-blocks -- and frees the slot, so
+// what a writer does after waiting for a TMEM slot is the same few stores for
+// every scale kind.  TMEM has room for four
 // scale slots (64 columns beside the two 224-column accumulators): K tile i
 // (counted over all of a pair's tiles) uses stage i / 2 % 3 and scale slot
 // i % 4.  The even CTA's `full[stage]` completes when both producers' loads
@@ -789,13 +787,11 @@ struct alignas(1024) SmemBsPair {
     alignas(128) uint8_t sa[kScaleSlots][kPairRows * 16];  // per row: four K tiles x 4 bytes (E8M0 x4 or one fp32)
     alignas(128) uint8_t sb[kScaleSlots][BN_BS * 16];
     uint64_t full[kBsPairStages], empty[kBsPairStages], tfull[2], tempty[2], drain;
-    uint64_t scale_full[kScaleSlots], scale_empty[kScaleSlots], scale_ready[kScaleSlots];
+    uint64_t scale_full[kScaleSlots], scale_empty[kScaleSlots];
     uint32_t tmem_base;
     int abort_flag;
     int bad_scale;
 };
-
-constexpr int kBsPairThreads = 352;  // producer, MMA, 4 epilogue, 4 scale-writer and 1 scale-converter warps
 
 // Scale-tensor TMA box of one group for an operand of kind KIND: the rows of the box and its bytes.
 template <int KIND>
@@ -823,55 +819,8 @@ __device__ __forceinline__ void sf_group_words(const uint8_t* slot, int r, int b
         w[jj] = KIND == SF_MX ? raw[jj] : e8m0_of_pow2(__uint_as_float(raw[jj]), bad) * 0x01010101u;
 }
 
-// The scale converter's work on one operand's slot of a group: fp32 block scales (powers of two) become
-// per-row E8M0 words in place, the layout of MX scales -- row r's word jj (the four 32-wide sub-blocks
-// of K tile jj) at byte 16 r + 4 jj -- for the slot's `nrows` rows.  A 128x128 box (one fp32 row per
-// 128 operand rows, block row 0 = operand row `row0` rounded down) is read first, then expanded to
-// every row.  Rows at or past `rows` get the neutral scale 1.  MX slots are left as they are.
-template <int KIND>
-__device__ __forceinline__ void sf_convert_slot(uint8_t* slot, int nrows, int64_t row0, int64_t rows, int lane,
-                                                uint32_t& bad) {
-    if constexpr (KIND == SF_ROW) {
-        for (int r = lane; r < nrows; r += 32) {
-            uint4* p = reinterpret_cast<uint4*>(slot + 16 * r);
-            if (row0 + r >= rows) {
-                *p = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-                continue;
-            }
-            const uint4 f = *p;
-            *p = make_uint4(e8m0_of_pow2(__uint_as_float(f.x), bad) * 0x01010101u,
-                            e8m0_of_pow2(__uint_as_float(f.y), bad) * 0x01010101u,
-                            e8m0_of_pow2(__uint_as_float(f.z), bad) * 0x01010101u,
-                            e8m0_of_pow2(__uint_as_float(f.w), bad) * 0x01010101u);
-        }
-    } else if constexpr (KIND == SF_BLOCK) {
-        // the box's block rows (at most three), converted by every lane, then written to every row
-        const int64_t b0 = row0 >> 7;
-        const int nblk = (int)(((row0 + nrows - 1) >> 7) - b0) + 1;
-        uint4 w[kScaleBlockRowsB];
-#pragma unroll
-        for (int b = 0; b < kScaleBlockRowsB; ++b) {
-            w[b] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-            if (b < nblk && ((b0 + b) << 7) < rows) {
-                const uint4 f = *reinterpret_cast<const uint4*>(slot + 16 * b);
-                w[b] = make_uint4(e8m0_of_pow2(__uint_as_float(f.x), bad) * 0x01010101u,
-                                  e8m0_of_pow2(__uint_as_float(f.y), bad) * 0x01010101u,
-                                  e8m0_of_pow2(__uint_as_float(f.z), bad) * 0x01010101u,
-                                  e8m0_of_pow2(__uint_as_float(f.w), bad) * 0x01010101u);
-            }
-        }
-        __syncwarp();  // every lane has read the box before any row is written over it
-        for (int r = lane; r < nrows; r += 32) {
-            const int b = (int)(((row0 + r) >> 7) - b0);
-            const uint4 v = row0 + r >= rows ? make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu)
-                                             : (b == 0 ? w[0] : b == 1 ? w[1] : w[2]);
-            *reinterpret_cast<uint4*>(slot + 16 * r) = v;
-        }
-    }
-}
-
 template <int OUT_BF16, int KA, int KB>
-__global__ void __launch_bounds__(kBsPairThreads, 1)
+__global__ void __launch_bounds__(320, 1)
     gemm_blockscaled_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                  const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                                  GemmArgs g, uint32_t idesc) {
@@ -884,7 +833,6 @@ __global__ void __launch_bounds__(kBsPairThreads, 1)
     volatile int* abort_flag = &S.abort_flag;
     constexpr int kSaBytes = scale_box_rows<KA>(kPairRows) * 16;
     constexpr int kSbBytes = scale_box_rows<KB>(BN_BS) * 16;
-    constexpr bool kConvert = KA != SF_MX || KB != SF_MX;  // fp32 block scales go through the converter
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBsPairStages; ++s) {
@@ -894,7 +842,6 @@ __global__ void __launch_bounds__(kBsPairThreads, 1)
         for (int s = 0; s < kScaleSlots; ++s) {
             mbar_init(smem_u32(&S.scale_full[s]), 1);
             mbar_init(smem_u32(&S.scale_empty[s]), 4);
-            mbar_init(smem_u32(&S.scale_ready[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&S.tfull[a]), 1);
@@ -1048,41 +995,12 @@ __global__ void __launch_bounds__(kBsPairThreads, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
-    } else if (warp == 10) {
-        // Scale converter: fp32 block scales of each group, rewritten in their ring slot as E8M0 words in
-        // the MX layout before the writers read them (nothing to do when both operands are MX).
-        if constexpr (kConvert) {
-            uint32_t bad = 0;
-            int gi = 0;  // scale groups converted (over all of this pair's tiles)
-            bool ok = true;
-            for (int t = cid; ok && t < g.num_tiles; t += ncl) {
-                int tm, tn;
-                tile_coords(t, g, tm, tn);
-                const int64_t arow0 = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows;
-                const int64_t brow0 = (int64_t)tn * BN_BS;
-                for (int grp = 0; grp < groups; ++grp, ++gi) {
-                    const int slot = gi % kScaleSlots;
-                    const bool w = mbar_wait_bounded(smem_u32(&S.scale_full[slot]), (uint32_t)((gi / kScaleSlots) & 1),
-                                                     abort_flag);
-                    if (!__all_sync(0xffffffffu, w)) {
-                        ok = false;
-                        break;
-                    }
-                    sf_convert_slot<KA>(S.sa[slot], kPairRows, arow0, g.M, lane, bad);
-                    sf_convert_slot<KB>(S.sb[slot], BN_BS, brow0, g.N, lane, bad);
-                    fence_proxy_async_smem();  // these stores precede the TMA load that later refills the slot
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&S.scale_ready[slot]));
-                }
-            }
-            if (__any_sync(0xffffffffu, bad != 0) && lane == 0) atomicOr(&S.bad_scale, 1);
-        }
     } else {
         // Scale writers of this CTA (warp 6..9 = lane quarter q): for every K tile, the A scale of row
         // 32q + lane (column q of the K tile's slot) and the scales of all 224 B rows (columns 8 + j).
-        // When a group's words are ready, each thread reads those of its rows for the group's four K
-        // tiles into registers and frees the ring slot; after each slot wait only the TMEM stores
-        // remain, the same for every scale kind.
+        // When a group's scales land, each thread reads the words of its rows for the group's four K
+        // tiles into registers (re-encoding fp32 block scales there) and frees the ring slot; after
+        // each slot wait only the TMEM stores remain, the same for every scale kind.
         const int q = warp & 3;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int kcount = 0;  // K tiles written so far (over all of this pair's tiles)
@@ -1097,19 +1015,18 @@ __global__ void __launch_bounds__(kBsPairThreads, 1)
             const int bblock = (tn * BN_BS) >> 7;
             for (int grp = 0; ok && grp < groups; ++grp) {  // k_tiles is a multiple of 4 on this path
                 const int slot = consumed % kScaleSlots;
-                // MX words are ready when they land; fp32 block scales once the converter has rewritten them
-                bool w = mbar_wait_bounded(smem_u32(kConvert ? &S.scale_ready[slot] : &S.scale_full[slot]),
-                                           (uint32_t)((consumed / kScaleSlots) & 1), abort_flag);
+                bool w = mbar_wait_bounded(smem_u32(&S.scale_full[slot]), (uint32_t)((consumed / kScaleSlots) & 1),
+                                           abort_flag);
                 if (!__all_sync(0xffffffffu, w)) {
                     ok = false;
                     break;
                 }
                 uint32_t wa[4], wb[kSfbCols][4];
-                sf_group_words<SF_MX>(S.sa[slot], q * 32 + lane, ablock, arow, g.M, wa, bad);
+                sf_group_words<KA>(S.sa[slot], q * 32 + lane, ablock, arow, g.M, wa, bad);
 #pragma unroll
                 for (int j = 0; j < kSfbCols; ++j)
-                    sf_group_words<SF_MX>(S.sb[slot], 32 * j + lane, bblock, (int64_t)tn * BN_BS + 32 * j + lane, g.N,
-                                          wb[j], bad);
+                    sf_group_words<KB>(S.sb[slot], 32 * j + lane, bblock, (int64_t)tn * BN_BS + 32 * j + lane, g.N,
+                                       wb[j], bad);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.scale_empty[slot]));  // the producer may refill the slot
                 ++consumed;
@@ -1303,7 +1220,7 @@ fp8_status launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmA
         const size_t smem_p = sizeof(SmemBsPair) + 1024;
         s = prepare_kernel(reinterpret_cast<const void*>(kp), smem_p);
         if (s != FP8_OK) return s;
-        return launch_pair_kernel(kp, smem_p, kBsPairThreads, st, tmA, tmB, tmSA, tmSB, g, idesc);
+        return launch_pair_kernel(kp, smem_p, 320, st, tmA, tmB, tmSA, tmSB, g, idesc);
     }
     const size_t smem = sizeof(SmemBS) + 1024;
     auto k = gemm_blockscaled_kernel<OUT_BF16, KA, KB>;
