@@ -305,6 +305,9 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
     }
     uint32_t amax_acc = 0;
     int cur_tr = (int)(first / a.tiles_c), cur_tc = (int)(first % a.tiles_c);  // tile being cast
+    const int64_t sf32_ld = cdiv(a.cols, 32);  // row pitch of 1x32 row scales
+    // every row's 16-column chunks are 16-byte aligned when the rows are (q_row is 8-byte aligned)
+    const bool rows16 = a.do_row && (a.cols % 16 == 0) && ((reinterpret_cast<uintptr_t>(a.q_row) & 15) == 0);
 
     for (int64_t i = 0; i < n_my; ++i, advance(cur_tr, cur_tc)) {
         if (tid == 0 && i >= 1 && i + 1 < n_my) {
@@ -365,9 +368,11 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
         // ---------------------------------------------------------- row-wise
         if (a.do_row) {
             const int64_t cc = c0 + 64 * rh + 16 * rcp;  // the thread's first column
+            const int64_t r_first = r0 + rl;
+            uint8_t* dst_row = a.q_row + r_first * a.cols + cc;  // advances 32 rows per visit
 #pragma unroll
-            for (int vi = 0; vi < 4; ++vi) {
-                const int64_t r = r0 + 32 * vi + rl;
+            for (int vi = 0; vi < 4; ++vi, dst_row += 32 * a.cols) {
+                const int64_t r = r_first + 32 * vi;
                 const bool row_ok = r < a.rows;
                 uint32_t s2;
                 if constexpr (GRAN == FP8_SCALE_TENSOR) {
@@ -379,7 +384,7 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
                     const int e = block_bias<GRAN>(m, FMT, a.margin);
                     s2 = pow2_bf16x2(e);
                     if ((rcp & 1) == 0 && row_ok && cc < a.cols)
-                        static_cast<uint8_t*>(a.sf_row)[r * cdiv(a.cols, 32) + (cc >> 5)] = (uint8_t)(127 - e);
+                        static_cast<uint8_t*>(a.sf_row)[r * sf32_ld + (cc >> 5)] = (uint8_t)(127 - e);
                 } else {  // 1x128
                     uint32_t m = max(pm[vi], __shfl_xor_sync(0xffffffffu, pm[vi], 1));
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
@@ -398,8 +403,8 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
                         q0 = encode8_f32<FMT>(v[vi][0], s_tensor);
                         q1 = encode8_f32<FMT>(v[vi][1], s_tensor);
                     }
-                    uint8_t* dst = a.q_row + r * a.cols + cc;
-                    if (cc + 16 <= a.cols && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                    uint8_t* dst = dst_row;
+                    if (cc + 16 <= a.cols && rows16) {
                         *reinterpret_cast<uint4*>(dst) = make_uint4(q0.x, q0.y, q1.x, q1.y);
                     } else {
                         if (cc < a.cols) *reinterpret_cast<uint2*>(dst) = q0;
