@@ -305,7 +305,7 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
     }
     uint32_t amax_acc = 0;
     int cur_tr = (int)(first / a.tiles_c), cur_tc = (int)(first % a.tiles_c);  // tile being cast
-    const int64_t sf32_ld = cdiv(a.cols, 32);  // row pitch of 1x32 row scales
+    const int64_t sf32_ld = cdiv(a.cols, 32), sf128_ld = a.tiles_c;  // row pitch of 1x32 / 1x128 row scales
     // every row's 16-column chunks are 16-byte aligned when the rows are (q_row is 8-byte aligned)
     const bool rows16 = a.do_row && (a.cols % 16 == 0) && ((reinterpret_cast<uintptr_t>(a.q_row) & 15) == 0);
 
@@ -392,7 +392,7 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
                     const int e = bias_bf16(m, FMT, a.margin);
                     s2 = pow2_bf16x2(e);
                     if (rh == 0 && rcp == 0 && row_ok)
-                        static_cast<float*>(a.sf_row)[r * cdiv(a.cols, kTile) + c0 / kTile] = pow2_exact(-e);
+                        static_cast<float*>(a.sf_row)[r * sf128_ld + cur_tc] = pow2_exact(-e);
                 }
                 if (row_ok) {
                     uint2 q0, q1;
