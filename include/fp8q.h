@@ -423,7 +423,8 @@ FP8Q_API fp8_status fp8_quantize_current_noalloc(const void *x, int64_t rows, in
  *                  unspecified result)
  *              (rows = M for A, N for B).  fp32 block scales must be powers of
  *              two in [2^-127, 2^127] (what fp8_quantize writes); any other
- *              value sets FP8_STATUS_BAD_BLOCK_SCALE.
+ *              value sets FP8_STATUS_BAD_BLOCK_SCALE, and D is then
+ *              unspecified.
  *   D        device, [M x N] fp32 or bf16 (out_dtype), leading dimension ldd
  *            (elements); 16-byte aligned, N and ldd multiples of 16.
  *   status   device int32 or NULL (FP8_STATUS_TIMEOUT, FP8_STATUS_BAD_BLOCK_SCALE).

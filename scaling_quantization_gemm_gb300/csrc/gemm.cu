@@ -799,14 +799,36 @@ __host__ __device__ constexpr int scale_box_rows(int rows) {
     return KIND == SF_BLOCK ? (rows == kPairRows ? 1 : kScaleBlockRowsB) : rows;
 }
 
+// Validity of fp32 block scales, accumulated without branches: a power of two in range is, after
+// 2^-127 (the only subnormal one) is mapped to the bit pattern of 2^-126, a pattern with sign and
+// mantissa clear between those of 2^-126 and 2^127.
+struct ScaleCheck {
+    uint32_t bits = 0, lo = 0xFFFFFFFFu, hi = 0;
+    __device__ __forceinline__ void add(uint32_t raw) {
+        const uint32_t u = raw == 0x00400000u ? 0x00800000u : raw;
+        bits |= u;
+        lo = min(lo, u);
+        hi = max(hi, u);
+    }
+    // true if some word added was not a power of two in [2^-127, 2^127]
+    __device__ __forceinline__ bool any_bad() const {
+        return (bits & 0x807FFFFFu) != 0 || lo < 0x00800000u || hi > 0x7F000000u;
+    }
+};
+
+// E8M0 code of an fp32 block scale that is a power of two in [2^-127, 2^127]: its biased exponent (0 for
+// 2^-127).  Other values give an unspecified code; they are found by the epilogue warps' check.
+__device__ __forceinline__ uint32_t e8m0_code(uint32_t raw) {
+    return raw == 0x00400000u ? 0u : (raw >> 23) & 0xFFu;
+}
+
 // The scale words of one operand row for the four K tiles of a scale group (word jj: four E8M0 bytes,
 // one per 32-wide K sub-block of K tile jj), from the group's shared-memory slot: MX words as they
-// are, fp32 block scales re-encoded (a value that is not a power of two sets `bad`).  Local row r of
-// the slot, or for 128x128 scales the block row of `row` counted from `block_base`; rows past the
-// edge get the neutral scale 1.
+// are, fp32 block scales as their E8M0 code.  Local row r of the slot, or for 128x128 scales the
+// block row of `row` counted from `block_base`; rows past the edge get the neutral scale 1.
 template <int KIND>
 __device__ __forceinline__ void sf_group_words(const uint8_t* slot, int r, int block_base, int64_t row, int64_t rows,
-                                               uint32_t (&w)[4], uint32_t& bad) {
+                                               uint32_t (&w)[4]) {
     if (row >= rows) {
         w[0] = w[1] = w[2] = w[3] = 0x7F7F7F7Fu;
         return;
@@ -815,8 +837,46 @@ __device__ __forceinline__ void sf_group_words(const uint8_t* slot, int r, int b
     const uint4 v = *reinterpret_cast<const uint4*>(slot + sr * 16);
     const uint32_t raw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
-        w[jj] = KIND == SF_MX ? raw[jj] : e8m0_of_pow2(__uint_as_float(raw[jj]), bad) * 0x01010101u;
+    for (int jj = 0; jj < 4; ++jj) w[jj] = KIND == SF_MX ? raw[jj] : e8m0_code(raw[jj]) * 0x01010101u;
+}
+
+// The epilogue warps' check of the fp32 block scales of pair tile (tm, tn), made from global memory
+// (L2) while they wait for the tile's accumulator: warp q of CTA `rank` checks the A scales of its 32
+// rows (1x128) or, warp 0, the CTA's one 128-row block (128x128), and the B scales of a quarter of the
+// CTA's half of the tile's rows (1x128) or, CTA 0's warps 0..2, the tile's 128-row blocks (128x128),
+// over all K tiles.  MX scales need no check (every E8M0 code but 255 is a scale).
+template <int KA, int KB>
+__device__ __forceinline__ bool tile_scales_bad(const GemmArgs& g, int tm, int tn, uint32_t rank, int q, int lane) {
+    ScaleCheck chk;
+    const int64_t arow0 = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows;
+    if constexpr (KA == SF_ROW) {
+        const int64_t row = arow0 + 32 * q + lane;
+        if (row < g.M) {
+            const uint32_t* p = static_cast<const uint32_t*>(g.sfa) + row * g.sfa_ld;
+            for (int k = 0; k < g.k_tiles; ++k) chk.add(__ldg(p + k));
+        }
+    } else if constexpr (KA == SF_BLOCK) {
+        if (q == 0 && arow0 < g.M) {
+            const uint32_t* p = static_cast<const uint32_t*>(g.sfa) + (arow0 >> 7) * g.sfa_ld;
+            for (int k = lane; k < g.k_tiles; k += 32) chk.add(__ldg(p + k));
+        }
+    }
+    if constexpr (KB == SF_ROW) {
+        const int local = 32 * q + lane;  // of this CTA's kBsPairB rows
+        const int64_t row = (int64_t)tn * BN_BS + (int64_t)rank * kBsPairB + local;
+        if (local < kBsPairB && row < g.N) {
+            const uint32_t* p = static_cast<const uint32_t*>(g.sfb) + row * g.sfb_ld;
+            for (int k = 0; k < g.k_tiles; ++k) chk.add(__ldg(p + k));
+        }
+    } else if constexpr (KB == SF_BLOCK) {
+        const int64_t b0 = ((int64_t)tn * BN_BS) >> 7, brow = b0 + q;
+        const int64_t last = ((int64_t)tn * BN_BS + BN_BS - 1) >> 7;
+        if (rank == 0 && q < kScaleBlockRowsB && brow <= last && (brow << 7) < g.N) {
+            const uint32_t* p = static_cast<const uint32_t*>(g.sfb) + brow * g.sfb_ld;
+            for (int k = lane; k < g.k_tiles; k += 32) chk.add(__ldg(p + k));
+        }
+    }
+    return chk.any_bad();
 }
 
 template <int OUT_BF16, int KA, int KB>
@@ -973,13 +1033,16 @@ __global__ void __launch_bounds__(320, 1)
         const int q = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
+        bool bad = false;
         for (int t = cid; t < g.num_tiles; t += ncl) {
+            int tm, tn;
+            tile_coords(t, g, tm, tn);
+            // fp32 block scales: checked here, off the MMAs' path, while the tile accumulates
+            if constexpr (KA != SF_MX || KB != SF_MX) bad |= tile_scales_bad<KA, KB>(g, tm, tn, rank, q, lane);
             bool ok = mbar_wait_bounded(smem_u32(&S.tfull[acc]), acc_phase, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            int tm, tn;
-            tile_coords(t, g, tm, tn);
             const int64_t row = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows + q * 32 + lane;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN_BS);
 #pragma unroll 1
@@ -995,6 +1058,7 @@ __global__ void __launch_bounds__(320, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&S.bad_scale, 1);
     } else {
         // Scale writers of this CTA (warp 6..9 = lane quarter q): for every K tile, the A scale of row
         // 32q + lane (column q of the K tile's slot) and the scales of all 224 B rows (columns 8 + j).
@@ -1022,11 +1086,11 @@ __global__ void __launch_bounds__(320, 1)
                     break;
                 }
                 uint32_t wa[4], wb[kSfbCols][4];
-                sf_group_words<KA>(S.sa[slot], q * 32 + lane, ablock, arow, g.M, wa, bad);
+                sf_group_words<KA>(S.sa[slot], q * 32 + lane, ablock, arow, g.M, wa);
 #pragma unroll
                 for (int j = 0; j < kSfbCols; ++j)
                     sf_group_words<KB>(S.sb[slot], 32 * j + lane, bblock, (int64_t)tn * BN_BS + 32 * j + lane, g.N,
-                                       wb[j], bad);
+                                       wb[j]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.scale_empty[slot]));  // the producer may refill the slot
                 ++consumed;

@@ -188,6 +188,30 @@ def test_gemm_bad_block_scale_sets_status(q):
     assert st == q.STATUS_BAD_BLOCK_SCALE
 
 
+@pytest.mark.parametrize("gb", [1, 2])
+def test_gemm_block_pair_kernel_edge_scales_and_bad_scale(q, gb):
+    """The CTA-pair block-scaled kernel (M > 128, K a multiple of 512) with fp32 block scales at the
+    ends of the E8M0 range (2^-127, 2^127) next to ordinary ones in the same rows (they take the
+    word-by-word conversion) matches the oracle exactly as usual; a scale that is not a power of two
+    raises FP8_STATUS_BAD_BLOCK_SCALE, also when it sits beside valid scales."""
+    rng = np.random.default_rng(40 + gb)
+    M, N, K = 512, 768, 1024
+    A, B = realistic_codes(rng, (M, K), 0), realistic_codes(rng, (N, K), 0)
+    sfa = pow2_scales(rng, (M, K // 128))
+    sfb = pow2_scales(rng, (N if gb == 1 else N // 128, K // 128))
+    sfa[5, 2], sfa[300, 0], sfb[1, 3] = np.float32(2.0 ** -127), np.float32(2.0 ** 127), np.float32(2.0 ** -127)
+    A[300, :128] = 0  # the 2^127 block multiplies zeros (any finite product of it would overflow fp32)
+    y, st = run_gemm(q, A, 0, 1, sfa, B, 0, gb, sfb, True)
+    assert st == 0
+    y_ref, mag = oracle.gemm_full(A, 0, 1, sfa, B, 0, gb, sfb)
+    assert_gemm_close(y, y_ref, mag, True)
+    for bad in (np.float32(0.3), np.float32(-2.0), np.float32(0.0), np.float32(np.inf)):
+        s2 = sfa.copy()
+        s2[200, 1] = bad
+        _, st = run_gemm(q, A, 0, 1, s2, B, 0, gb, sfb, True)
+        assert st == q.STATUS_BAD_BLOCK_SCALE, bad
+
+
 @pytest.mark.parametrize("out_bf16", [False, True])
 def test_gemm_nan_operand_poisons_its_row_only(q, out_bf16):
     """A NaN code in A makes its output row NaN (the fp64 oracle agrees); every other row is finite
