@@ -59,8 +59,20 @@ constexpr int kGroupM = 16;  // tile raster: groups of 16 M-tiles walk N togethe
 constexpr int BN_BS = 224;
 constexpr int kBBytesBS = BN_BS * BK;
 constexpr int kSfColBase = 2 * BN_BS;  // scale slots start after the two accumulators (448)
-constexpr int kSfColsPerStage = 16;    // A scales at +0 (4 columns), B scales at +8 (7 columns)
-constexpr int kSfbCols = BN_BS / 32;
+constexpr int kSfColsPerStage = 16;    // A scales at +0 (4 columns), B scales at +8 (up to 8 columns)
+constexpr int kSfbCols = (BN_BS + 31) / 32;
+static_assert(kSfbCols <= 8, "B scales of a tile fill at most eight TMEM columns");
+
+// Block-scaled CTA-pair kernel: pair tile width and TMEM layout (accumulators, then scale slots).
+// Measured on the MXFP8 and per-block shapes: 224 columns with two accumulators beat 192 with eight
+// scale slots and 256 with one accumulator (the block-scaled MMAs cost about the same per stage
+// beyond their arithmetic whatever the width, so narrower tiles lose and one accumulator exposes the
+// epilogue).
+constexpr int kBnPair = 224;   // output columns (B rows) of a pair tile
+constexpr int kAccBufs = 2;    // accumulators: with two, a tile's epilogue overlaps the next tile's MMAs
+constexpr int kSfColBasePair = kAccBufs * kBnPair;
+constexpr int kSfbColsPair = (kBnPair + 31) / 32;
+static_assert(kSfbColsPair <= 8, "B scales of a tile fill at most eight TMEM columns");
 
 enum { SF_MX = 0, SF_ROW = 1, SF_BLOCK = 2 };  // E8M0 1x32 | fp32 per row (1x128) | fp32 per 128 rows (128x128)
 
@@ -690,7 +702,8 @@ __global__ void __launch_bounds__(320, 1)
                 uint32_t wb[8];
 #pragma unroll
                 for (int j = 0; j < kSfbCols; ++j) wb[j] = sf_word<KB>(comp(src.b[j], jj), bad);
-                wb[7] = 0x7F7F7F7Fu;
+#pragma unroll
+                for (int j = kSfbCols; j < 8; ++j) wb[j] = 0x7F7F7F7Fu;
                 tmem_st_32x32b_x8(slot + 8, wb);
                 tmem_st_wait();
                 tc_fence_before();
@@ -772,20 +785,29 @@ __global__ void __launch_bounds__(320, 1)
 // tiles past i.
 constexpr int kBsKPerStage = 2;  // 128-wide K tiles per operand stage
 constexpr int kBsPairStages = 3;
-constexpr int kSfSlots = 4;  // TMEM scale slots (kSfColsPerStage columns each)
-constexpr int kBsPairB = BN_BS / 2;                    // 112 rows of B per CTA
+constexpr int kSfSlots = (512 - kSfColBasePair) / kSfColsPerStage;  // TMEM scale slots beside the accumulators
+constexpr int kSfRing = kSfSlots / kBsKPerStage;                     // stage steps the scale slots hold
+static_assert(kSfSlots % kBsKPerStage == 0 && kSfRing >= 2, "scale slots hold whole stage steps");
+// The writers of stage step s wait until the MMAs of step s - kSfAhead are done: by then the slots of
+// step s are free (their last reader, step s - kSfRing, is done) and `full[s % kBsPairStages]` has
+// completed the phase of step s - kBsPairStages, so their arrivals count toward step s.  Running them
+// further ahead than the operand ring lets an arrival land on a phase still open (a version that did
+// faulted the GPU).
+constexpr int kSfAhead = kSfRing < kBsPairStages ? kSfRing : kBsPairStages;
+constexpr int kBsPairB = kBnPair / 2;                    // rows of B per CTA
 constexpr int kBsPairABytes = kPairRows * BK;          // 16 KB per K tile
-constexpr int kBsPairBBytes = kBsPairB * BK;           // 14 KB per K tile
+constexpr int kBsPairBBytes = kBsPairB * BK;           // B bytes per K tile and CTA
 constexpr int kBsPairStageBytes = kBsKPerStage * (kBsPairABytes + kBsPairBBytes);
 constexpr int kScaleSlots = 4;
 constexpr int kScaleAhead = 2;  // scale groups loaded ahead of the group being consumed
-constexpr int kScaleBlockRowsB = 3;                    // 224 B rows touch at most three 128-row blocks
+constexpr int kScaleBlockRowsB = 3;                    // a tile's B rows touch at most three 128-row blocks
+static_assert(kBnPair <= 2 * 128 + 1, "a tile's B rows span at most three 128-row blocks");
 
 struct alignas(1024) SmemBsPair {
     uint8_t a[kBsPairStages][kBsKPerStage * kBsPairABytes];
     uint8_t b[kBsPairStages][kBsKPerStage * kBsPairBBytes];
     alignas(128) uint8_t sa[kScaleSlots][kPairRows * 16];  // per row: four K tiles x 4 bytes (E8M0 x4 or one fp32)
-    alignas(128) uint8_t sb[kScaleSlots][BN_BS * 16];
+    alignas(128) uint8_t sb[kScaleSlots][kBnPair * 16];
     uint64_t full[kBsPairStages], empty[kBsPairStages], tfull[2], tempty[2], drain;
     uint64_t scale_full[kScaleSlots], scale_empty[kScaleSlots];
     uint32_t tmem_base;
@@ -863,14 +885,14 @@ __device__ __forceinline__ bool tile_scales_bad(const GemmArgs& g, int tm, int t
     }
     if constexpr (KB == SF_ROW) {
         const int local = 32 * q + lane;  // of this CTA's kBsPairB rows
-        const int64_t row = (int64_t)tn * BN_BS + (int64_t)rank * kBsPairB + local;
+        const int64_t row = (int64_t)tn * kBnPair + (int64_t)rank * kBsPairB + local;
         if (local < kBsPairB && row < g.N) {
             const uint32_t* p = static_cast<const uint32_t*>(g.sfb) + row * g.sfb_ld;
             for (int k = 0; k < g.k_tiles; ++k) chk.add(__ldg(p + k));
         }
     } else if constexpr (KB == SF_BLOCK) {
-        const int64_t b0 = ((int64_t)tn * BN_BS) >> 7, brow = b0 + q;
-        const int64_t last = ((int64_t)tn * BN_BS + BN_BS - 1) >> 7;
+        const int64_t b0 = ((int64_t)tn * kBnPair) >> 7, brow = b0 + q;
+        const int64_t last = ((int64_t)tn * kBnPair + kBnPair - 1) >> 7;
         if (rank == 0 && q < kScaleBlockRowsB && brow <= last && (brow << 7) < g.N) {
             const uint32_t* p = static_cast<const uint32_t*>(g.sfb) + brow * g.sfb_ld;
             for (int k = lane; k < g.k_tiles; k += 32) chk.add(__ldg(p + k));
@@ -892,7 +914,7 @@ __global__ void __launch_bounds__(320, 1)
     const int groups = (g.k_tiles + 3) / 4;
     volatile int* abort_flag = &S.abort_flag;
     constexpr int kSaBytes = scale_box_rows<KA>(kPairRows) * 16;
-    constexpr int kSbBytes = scale_box_rows<KB>(BN_BS) * 16;
+    constexpr int kSbBytes = scale_box_rows<KB>(kBnPair) * 16;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBsPairStages; ++s) {
@@ -903,7 +925,7 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(smem_u32(&S.scale_full[s]), 1);
             mbar_init(smem_u32(&S.scale_empty[s]), 4);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kAccBufs; ++a) {
             mbar_init(smem_u32(&S.tfull[a]), 1);
             mbar_init(smem_u32(&S.tempty[a]), 8);
         }
@@ -943,7 +965,7 @@ __global__ void __launch_bounds__(320, 1)
                 int tm, tn;
                 tile_coords(nt, g, tm, tn);
                 const int xa = KA == SF_MX ? 16 * ngrp : 4 * ngrp, xb = KB == SF_MX ? 16 * ngrp : 4 * ngrp;
-                const int arow = tm * kPairTile + (int)rank * kPairRows, brow = tn * BN_BS;
+                const int arow = tm * kPairTile + (int)rank * kPairRows, brow = tn * kBnPair;
                 mbar_arrive_expect_tx(smem_u32(&S.scale_full[slot]), kSaBytes + kSbBytes);
                 tma_load_2d(smem_u32(S.sa[slot]), &tmSA, smem_u32(&S.scale_full[slot]), xa, KA == SF_BLOCK ? arow >> 7 : arow);
                 tma_load_2d(smem_u32(S.sb[slot]), &tmSB, smem_u32(&S.scale_full[slot]), xb, KB == SF_BLOCK ? brow >> 7 : brow);
@@ -970,7 +992,7 @@ __global__ void __launch_bounds__(320, 1)
                         tma_load_2d_pair(smem_u32(S.a[stage] + h * kBsPairABytes), &tmA, full_leader, (kt + h) * BK,
                                          tm * kPairTile + (int)rank * kPairRows);
                         tma_load_2d_pair(smem_u32(S.b[stage] + h * kBsPairBBytes), &tmB, full_leader, (kt + h) * BK,
-                                         tn * BN_BS + (int)rank * kBsPairB);
+                                         tn * kBnPair + (int)rank * kBsPairB);
                     }
                     mbar_arrive_expect_tx_cluster(full_leader, kBsPairStageBytes);
                     if (++stage == kBsPairStages) {
@@ -993,7 +1015,7 @@ __global__ void __launch_bounds__(320, 1)
             for (int t = cid; ok && t < g.num_tiles; t += ncl) {
                 if (!mbar_wait_bounded(smem_u32(&S.tempty[acc]), acc_phase ^ 1, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(acc * BN_BS);
+                const uint32_t d = tmem + (uint32_t)(acc * kBnPair);
                 for (int kt = 0; kt < g.k_tiles; kt += kBsKPerStage) {
                     if (!mbar_wait_bounded(smem_u32(&S.full[stage]), phase, abort_flag)) {
                         ok = false;
@@ -1004,7 +1026,7 @@ __global__ void __launch_bounds__(320, 1)
                     for (int h = 0; h < kBsKPerStage; ++h) {
                         const uint64_t ad = sdesc_kmajor_sw128(smem_u32(S.a[stage] + h * kBsPairABytes));
                         const uint64_t bd = sdesc_kmajor_sw128(smem_u32(S.b[stage] + h * kBsPairBBytes));
-                        const uint32_t sfa_t = tmem + (uint32_t)(kSfColBase + slot * kSfColsPerStage);
+                        const uint32_t sfa_t = tmem + (uint32_t)(kSfColBasePair + slot * kSfColsPerStage);
                         const uint32_t sfb_t = sfa_t + 8;
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k)
@@ -1021,8 +1043,10 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 if (!ok) break;
                 tc_commit_pair_multicast(smem_u32(&S.tfull[acc]), 0x3);
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1;
+                if (++acc == kAccBufs) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
             }
             tc_commit_pair(smem_u32(&S.drain));
             const uint64_t t0 = globaltimer_ns();
@@ -1044,19 +1068,21 @@ __global__ void __launch_bounds__(320, 1)
             if (!ok) break;
             tc_fence_after();
             const int64_t row = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows + q * 32 + lane;
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN_BS);
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBnPair);
 #pragma unroll 1
-            for (int c = 0; c < BN_BS / 32; ++c) {
+            for (int c = 0; c < kBnPair / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
-                const int64_t col0 = (int64_t)tn * BN_BS + c * 32;
+                const int64_t col0 = (int64_t)tn * kBnPair + c * 32;
                 if (row < g.M) store_row32<OUT_BF16>(g, row, col0, r, 1.0f, 1.0f);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&S.tempty[acc]), 0));
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1;
+            if (++acc == kAccBufs) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&S.bad_scale, 1);
     } else {
@@ -1076,7 +1102,7 @@ __global__ void __launch_bounds__(320, 1)
             tile_coords(t, g, tm, tn);
             const int64_t arow = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows + q * 32 + lane;
             const int ablock = (tm * kPairTile + (int)rank * kPairRows) >> 7;
-            const int bblock = (tn * BN_BS) >> 7;
+            const int bblock = (tn * kBnPair) >> 7;
             for (int grp = 0; ok && grp < groups; ++grp) {  // k_tiles is a multiple of 4 on this path
                 const int slot = consumed % kScaleSlots;
                 bool w = mbar_wait_bounded(smem_u32(&S.scale_full[slot]), (uint32_t)((consumed / kScaleSlots) & 1),
@@ -1085,19 +1111,19 @@ __global__ void __launch_bounds__(320, 1)
                     ok = false;
                     break;
                 }
-                uint32_t wa[4], wb[kSfbCols][4];
+                uint32_t wa[4], wb[kSfbColsPair][4];
                 sf_group_words<KA>(S.sa[slot], q * 32 + lane, ablock, arow, g.M, wa);
 #pragma unroll
-                for (int j = 0; j < kSfbCols; ++j)
-                    sf_group_words<KB>(S.sb[slot], 32 * j + lane, bblock, (int64_t)tn * BN_BS + 32 * j + lane, g.N,
+                for (int j = 0; j < kSfbColsPair; ++j)
+                    sf_group_words<KB>(S.sb[slot], 32 * j + lane, bblock, (int64_t)tn * kBnPair + 32 * j + lane, g.N,
                                        wb[j]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.scale_empty[slot]));  // the producer may refill the slot
                 ++consumed;
 #pragma unroll
                 for (int u = 0; u < 4 / kBsKPerStage; ++u) {  // one stage (two K tiles) per arrival
-                    if (kcount >= kSfSlots) {  // the MMAs of K tiles kcount - 4 and - 3 are done with the slots
-                        const int prev = (kcount - kSfSlots) / kBsKPerStage;  // the stage step that held them
+                    if (kcount >= kSfAhead * kBsKPerStage) {
+                        const int prev = kcount / kBsKPerStage - kSfAhead;  // its MMAs must be done
                         w = mbar_wait_bounded(smem_u32(&S.empty[prev % kBsPairStages]),
                                               (uint32_t)((prev / kBsPairStages) & 1), abort_flag);
                         if (!__all_sync(0xffffffffu, w)) {
@@ -1111,12 +1137,13 @@ __global__ void __launch_bounds__(320, 1)
                     for (int h = 0; h < kBsKPerStage; ++h) {
                         const int jj = kBsKPerStage * u + h;
                         const uint32_t tslot =
-                            tmem + lane_base + (uint32_t)(kSfColBase + ((kcount + h) % kSfSlots) * kSfColsPerStage);
+                            tmem + lane_base + (uint32_t)(kSfColBasePair + ((kcount + h) % kSfSlots) * kSfColsPerStage);
                         tmem_st_32x32b_x1(tslot + q, wa[jj]);
                         uint32_t v8[8];
 #pragma unroll
-                        for (int j = 0; j < kSfbCols; ++j) v8[j] = wb[j][jj];
-                        v8[7] = 0x7F7F7F7Fu;
+                        for (int j = 0; j < kSfbColsPair; ++j) v8[j] = wb[j][jj];
+#pragma unroll
+                        for (int j = kSfbColsPair; j < 8; ++j) v8[j] = 0x7F7F7F7Fu;
                         tmem_st_32x32b_x8(tslot + 8, v8);
                     }
                     tmem_st_wait();
@@ -1278,7 +1305,7 @@ fp8_status launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmA
         CUtensorMap tmSA, tmSB;
         fp8_status s = make_scale_map<KA>(&tmSA, g.sfa, g.M, g.sfa_ld, kPairRows);
         if (s != FP8_OK) return s;
-        s = make_scale_map<KB>(&tmSB, g.sfb, g.N, g.sfb_ld, BN_BS);
+        s = make_scale_map<KB>(&tmSB, g.sfb, g.N, g.sfb_ld, kBnPair);
         if (s != FP8_OK) return s;
         auto kp = gemm_blockscaled_pair_kernel<OUT_BF16, KA, KB>;
         const size_t smem_p = sizeof(SmemBsPair) + 1024;
@@ -1324,7 +1351,7 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
     // scale rows, which needs K % 512 == 0 and 16-byte aligned scale tensors
     const bool pair = M > BM && (!blockscaled || (K % 512 == 0 && (reinterpret_cast<uintptr_t>(sfa) & 15) == 0 &&
                                                   (reinterpret_cast<uintptr_t>(sfb) & 15) == 0));
-    const int bn = blockscaled ? BN_BS : BN;
+    const int bn = blockscaled ? (pair ? kBnPair : BN_BS) : BN;
     GemmArgs g;
     g.M = (int)M;
     g.N = (int)N;
@@ -1386,7 +1413,7 @@ fp8_status launch_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_
     };
     g.vec_a = vec_ok(sfa, ga, g.sfa_ld);
     g.vec_b = vec_ok(sfb, gb, g.sfb_ld);
-    const uint32_t idesc = idesc_mxf8f6f4(fa, fb, pair ? kPairTile : BM, BN_BS, 0, 0);
+    const uint32_t idesc = idesc_mxf8f6f4(fa, fb, pair ? kPairTile : BM, pair ? kBnPair : BN_BS, 0, 0);
     return out_bf16 ? dispatch_bs<1>(sf_kind(ga), sf_kind(gb), tmA, tmB, g, idesc, grid, st)
                     : dispatch_bs<0>(sf_kind(ga), sf_kind(gb), tmA, tmB, g, idesc, grid, st);
 }

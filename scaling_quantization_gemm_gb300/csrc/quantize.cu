@@ -77,8 +77,11 @@ __device__ __forceinline__ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 
 // (m > 1.75 <=> the 7 fraction bits exceed 0x60); other m take the general path.
 __device__ __forceinline__ int bias_bf16(uint32_t m, int fmt, int margin) {
     if (m - 0x80u < 0x7F00u) {
+        // floor(log2(fmax / amax)) with fmax = 1.75 * 2^ef and amax = (1 + f) 2^(E - 127): ef + 127 - E, one
+        // less when f > 0.75 (a mantissa above 0x60), and adding 0x1F to the bits carries into the
+        // exponent field exactly then
         const int ef = fmt == FP8_E4M3 ? 8 : 15;
-        int e = ef + 127 - (int)(m >> 7) - ((m & 0x7Fu) > 0x60u ? 1 : 0) - margin;
+        const int e = ef + 127 - margin - (int)((m + 0x1Fu) >> 7);
         return min(max(e, -126), 127);
     }
     bool nf = false;
@@ -370,8 +373,10 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
             const int64_t cc = c0 + 64 * rh + 16 * rcp;  // the thread's first column
             const int64_t r_first = r0 + rl;
             uint8_t* dst_row = a.q_row + r_first * a.cols + cc;  // advances 32 rows per visit
+            // MX: the E8M0 byte of the thread's 32-column block (lanes with even rcp store it)
+            uint8_t* sf_mx = kMX ? static_cast<uint8_t*>(a.sf_row) + r_first * sf32_ld + (cc >> 5) : nullptr;
 #pragma unroll
-            for (int vi = 0; vi < 4; ++vi, dst_row += 32 * a.cols) {
+            for (int vi = 0; vi < 4; ++vi, dst_row += 32 * a.cols, sf_mx += kMX ? 32 * sf32_ld : 0) {
                 const int64_t r = r_first + 32 * vi;
                 const bool row_ok = r < a.rows;
                 uint32_t s2;
@@ -383,8 +388,7 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
                     const uint32_t m = max(pm[vi], __shfl_xor_sync(0xffffffffu, pm[vi], 1));
                     const int e = block_bias<GRAN>(m, FMT, a.margin);
                     s2 = pow2_bf16x2(e);
-                    if ((rcp & 1) == 0 && row_ok && cc < a.cols)
-                        static_cast<uint8_t*>(a.sf_row)[r * sf32_ld + (cc >> 5)] = (uint8_t)(127 - e);
+                    if ((rcp & 1) == 0 && row_ok && cc < a.cols) *sf_mx = (uint8_t)(127 - e);
                 } else {  // 1x128
                     uint32_t m = max(pm[vi], __shfl_xor_sync(0xffffffffu, pm[vi], 1));
                     m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));

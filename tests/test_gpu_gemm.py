@@ -212,6 +212,28 @@ def test_gemm_block_pair_kernel_edge_scales_and_bad_scale(q, gb):
         assert st == q.STATUS_BAD_BLOCK_SCALE, bad
 
 
+@pytest.mark.parametrize("w,ga,gb", [(32, 1, 2), (48, 1, 1), (112, 3, 3), (192, 1, 2), (208, 1, 2), (16, 3, 3)])
+def test_gemm_block_pair_ragged_last_column(q, w, ga, gb):
+    """The CTA-pair block-scaled kernel with a last tile column w columns wide (N = 4 x 224 + w) and
+    80 pair tiles, more than the grid's pairs (a second, partial round of the persistent loop).
+    Every output element is written (D starts as NaN); sampled rows of every tile row, and all the
+    rows of the last tile row, match the oracle."""
+    rng = np.random.default_rng(60 + w + ga)
+    M, N, K = 4096, 4 * 224 + w, 512
+    A, B = realistic_codes(rng, (M, K), 0), realistic_codes(rng, (N, K), 0)
+    if ga == 3:
+        sfa, sfb = mx_scales(rng, M, K), mx_scales(rng, N, K)
+    else:
+        sfa = pow2_scales(rng, (M, K // 128))
+        sfb = pow2_scales(rng, (N if gb == 1 else -(-N // 128), K // 128))
+    y, st = run_gemm(q, A, 0, ga, sfa, B, 0, gb, sfb, True)
+    assert st == 0
+    assert not np.isnan(y).any(), "an output tile was not written"
+    rows = np.unique(np.concatenate([np.arange(0, M, 37), np.arange(M - 256, M, 5), [M - 1]]))
+    y_ref, mag = oracle.gemm_full(A[rows], 0, ga, sfa[rows], B, 0, gb, sfb)
+    assert_gemm_close(y[rows], y_ref, mag, True)
+
+
 @pytest.mark.parametrize("out_bf16", [False, True])
 def test_gemm_nan_operand_poisons_its_row_only(q, out_bf16):
     """A NaN code in A makes its output row NaN (the fp64 oracle agrees); every other row is finite
