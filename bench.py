@@ -662,17 +662,28 @@ def cpu_baseline(host, step_flops: float, R: int = 512):
     o.lib()
     flops, sec = oracle_step_sample(host, R, ffn_scales(host))
     cores = o.max_threads()
-    # the oracle's casts (per-tensor and MX, row + column-wise) on one thread and on all cores, over
-    # 1024 rows of the FFN gradient (21 M elements); GB/s of algorithmic bytes as for the GPU casts
+    # the oracle's casts in every mode (per-tensor, 1x128, 128x128, MX 1x32; row + column-wise) on one
+    # thread and on all cores, over 1024 rows of the FFN gradient (21 M elements); GB/s of algorithmic
+    # bytes as for the GPU casts (2 B read + 1 B per copy written + the scale bytes)
     xs = np.ascontiguousarray(host["dY5"][:1024])
     scale = o.scale_triple(o.amax(xs), 1, 1)[1]
-    cast_rates = {}
+    modes = (("tensor", None, 4.0), ("1x128", o.BLOCK_1x128, 4.0 + 8.0 / 128),
+             ("128x128", o.BLOCK_128x128, 4.0 + 8.0 / 16384), ("mx_1x32", o.MX_1x32, 4.0 + 2.0 / 32))
+    cast_rates, by_mode = {}, {}
     for nthreads in (1, cores):
         o.set_threads(nthreads)
-        t0 = time.time()
-        o.quantize_tensor(xs, 1, scale, row=True, col=True)
-        o.quantize_block(xs, 1, o.MX_1x32, 0, row=True, col=True)
-        cast_rates[nthreads] = (4.0 + 4.0 + 2.0 / 32) * xs.size / (time.time() - t0) / 1e9
+        total_b, total_s = 0.0, 0.0
+        for name, gran, bpe in modes:
+            t0 = time.time()
+            if gran is None:
+                o.quantize_tensor(xs, 1, scale, row=True, col=True)
+            else:
+                o.quantize_block(xs, 1, gran, 0, row=True, col=True)
+            dt = time.time() - t0
+            by_mode.setdefault(name, {})[str(nthreads)] = round(bpe * xs.size / dt / 1e9, 3)
+            total_b += bpe * xs.size
+            total_s += dt
+        cast_rates[nthreads] = total_b / total_s / 1e9
     o.set_threads(cores)
     value = flops / sec
     return {"value": round(value / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
@@ -681,7 +692,9 @@ def cpu_baseline(host, step_flops: float, R: int = 512):
                       f"history); {flops / 1e9:.2f} GFLOP in {sec:.1f} s",
             "extrapolated_full_step_s": round(step_flops / value, 1),
             "cast_gbs_1_thread": round(cast_rates[1], 3), "cast_gbs_all_cores": round(cast_rates[cores], 3),
-            "cast_sample": "per-tensor and MX casts, row + column-wise, of 1024 x 20480 bf16 (the FFN gradient)"}
+            "cast_gbs_by_mode": by_mode,
+            "cast_sample": "casts in every mode (per-tensor, 1x128, 128x128, MX 1x32), row + column-wise, of "
+                           "1024 x 20480 bf16 (the FFN gradient); the keys of cast_gbs_by_mode are thread counts"}
 
 
 def run_reference(args, rank, world):
