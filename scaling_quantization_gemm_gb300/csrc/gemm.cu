@@ -771,7 +771,7 @@ __global__ void __launch_bounds__(320, 1)
 // as they are; power-of-two fp32 block scales (1x128, 128x128) re-encoded as
 // E8M0 and repeated over the four 32-wide sub-blocks -- and frees the slot, so
 // what a writer does after waiting for a TMEM slot is the same few stores for
-// every scale kind.  TMEM has room for four
+// every scale kind.  With 224-column tiles and two accumulators TMEM has room for four
 // scale slots (64 columns beside the two 224-column accumulators): K tile i
 // (counted over all of a pair's tiles) uses stage i / 2 % 3 and scale slot
 // i % 4.  The even CTA's `full[stage]` completes when both producers' loads
@@ -791,8 +791,8 @@ static_assert(kSfSlots % kBsKPerStage == 0 && kSfRing >= 2, "scale slots hold wh
 // The writers of stage step s wait until the MMAs of step s - kSfAhead are done: by then the slots of
 // step s are free (their last reader, step s - kSfRing, is done) and `full[s % kBsPairStages]` has
 // completed the phase of step s - kBsPairStages, so their arrivals count toward step s.  Running them
-// further ahead than the operand ring lets an arrival land on a phase still open (a version that did
-// faulted the GPU).
+// further ahead than the operand ring would let an arrival land on a phase still open, one more than the
+// barrier's count (undefined behaviour; on the GPU, a fault).  With the constants above kSfAhead = 2.
 constexpr int kSfAhead = kSfRing < kBsPairStages ? kSfRing : kBsPairStages;
 constexpr int kBsPairB = kBnPair / 2;                    // rows of B per CTA
 constexpr int kBsPairABytes = kPairRows * BK;          // 16 KB per K tile
