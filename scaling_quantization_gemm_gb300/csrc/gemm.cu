@@ -801,6 +801,10 @@ constexpr int kBsPairStageBytes = kBsKPerStage * (kBsPairABytes + kBsPairBBytes)
 constexpr int kScaleSlots = 4;
 constexpr int kScaleAhead = 2;  // scale groups loaded ahead of the group being consumed
 constexpr int kScaleBlockRowsB = 3;                    // a tile's B rows touch at most three 128-row blocks
+// Epilogue staging for TMA stores of D: per warp 32 rows x 32 columns, as two 2 KB halves for bf16
+// (alternating chunks) or one 4 KB buffer for fp32; rows in the 64-byte (bf16) or 128-byte (fp32)
+// swizzle of the store's tensor map.
+constexpr int kOutStageBytes = 4096;
 static_assert(kBnPair <= 2 * 128 + 1, "a tile's B rows span at most three 128-row blocks");
 
 struct alignas(1024) SmemBsPair {
@@ -808,12 +812,15 @@ struct alignas(1024) SmemBsPair {
     uint8_t b[kBsPairStages][kBsKPerStage * kBsPairBBytes];
     alignas(128) uint8_t sa[kScaleSlots][kPairRows * 16];  // per row: four K tiles x 4 bytes (E8M0 x4 or one fp32)
     alignas(128) uint8_t sb[kScaleSlots][kBnPair * 16];
+    alignas(1024) uint8_t out[4][kOutStageBytes];  // per epilogue warp: staged output chunks for TMA stores
     uint64_t full[kBsPairStages], empty[kBsPairStages], tfull[2], tempty[2], drain;
     uint64_t scale_full[kScaleSlots], scale_empty[kScaleSlots];
     uint32_t tmem_base;
     int abort_flag;
     int bad_scale;
 };
+
+static_assert(sizeof(SmemBsPair) + 1024 <= 232448, "the pair kernel's shared memory fits one SM (227 KB)");
 
 // Scale-tensor TMA box of one group for an operand of kind KIND: the rows of the box and its bytes.
 template <int KIND>
@@ -905,7 +912,7 @@ template <int OUT_BF16, int KA, int KB>
 __global__ void __launch_bounds__(320, 1)
     gemm_blockscaled_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                  const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                                 GemmArgs g, uint32_t idesc) {
+                                 const __grid_constant__ CUtensorMap tmD, GemmArgs g, uint32_t idesc) {
     extern __shared__ uint8_t smem_raw[];
     SmemBsPair& S = *reinterpret_cast<SmemBsPair*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -937,6 +944,7 @@ __global__ void __launch_bounds__(320, 1)
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmSA);
         tma_prefetch_desc(&tmSB);
+        tma_prefetch_desc(&tmD);
     }
     cluster_sync_all();
     if (warp == 1) {
@@ -1058,6 +1066,8 @@ __global__ void __launch_bounds__(320, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool bad = false;
+        const uint32_t obuf = smem_u32(S.out[q]);
+        uint32_t nchunk = 0;  // chunks this warp has staged (bf16 alternates the two halves of its buffer)
         for (int t = cid; t < g.num_tiles; t += ncl) {
             int tm, tn;
             tile_coords(t, g, tm, tn);
@@ -1067,14 +1077,42 @@ __global__ void __launch_bounds__(320, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const int64_t row = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows + q * 32 + lane;
+            const int64_t row0 = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows + q * 32;  // this warp's rows
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBnPair);
 #pragma unroll 1
             for (int c = 0; c < kBnPair / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
                 const int64_t col0 = (int64_t)tn * kBnPair + c * 32;
-                if (row < g.M) store_row32<OUT_BF16>(g, row, col0, r, 1.0f, 1.0f);
+                {
+                    // stage row `lane` of the 32 x 32 chunk, then one TMA store per warp (clipped at the edges)
+                    const uint32_t buf = obuf + (OUT_BF16 ? (nchunk & 1u) * 2048u : 0u);
+                    ++nchunk;
+                    if (lane == 0) bulk_wait_read<OUT_BF16 ? 1 : 0>();  // the store that last read `buf` is done
+                    __syncwarp();
+                    if constexpr (OUT_BF16) {
+                        const uint32_t line = buf + (uint32_t)lane * 64u;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            st_shared_v4(line + ((uint32_t)(j ^ ((lane >> 1) & 3)) << 4),
+                                         cvt_bf16x2(__uint_as_float(r[8 * j]), __uint_as_float(r[8 * j + 1])),
+                                         cvt_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                                         cvt_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                                         cvt_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+                    } else {
+                        const uint32_t line = buf + (uint32_t)lane * 128u;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            st_shared_v4(line + ((uint32_t)(j ^ (lane & 7)) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2],
+                                         r[4 * j + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (row0 < g.M && col0 < g.N) tma_store_2d(&tmD, buf, (int)col0, (int)row0);
+                        bulk_commit();
+                    }
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -1084,6 +1122,7 @@ __global__ void __launch_bounds__(320, 1)
                 acc_phase ^= 1;
             }
         }
+        if (lane == 0) bulk_wait_all();  // this warp's stores are complete before the CTA exits
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&S.bad_scale, 1);
     } else {
         // Scale writers of this CTA (warp 6..9 = lane quarter q): for every K tile, the A scale of row
@@ -1197,6 +1236,23 @@ fp8_status make_operand_map(CUtensorMap* map, const void* ptr, int64_t rows, int
     return FP8_OK;
 }
 
+// 2-D map over the output D [M x N] (row pitch ldd elements) for the pair epilogue's TMA stores: box 32 x 32,
+// rows of the box in the 64-byte (bf16) or 128-byte (fp32) swizzle.
+fp8_status make_out_map(CUtensorMap* map, void* ptr, int64_t M, int64_t N, int64_t ldd, bool bf16) {
+    auto fn = encode_fn();
+    FP8_REQUIRE(fn != nullptr, FP8_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    const int64_t es = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldd * es)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    FP8_REQUIRE(r == CUDA_SUCCESS, FP8_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", (int)r);
+    return FP8_OK;
+}
+
 // Raise the dynamic shared-memory limit of `func` once per (function, device).
 fp8_status prepare_kernel(const void* func, size_t smem) {
     static std::mutex mu;
@@ -1307,11 +1363,14 @@ fp8_status launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmA
         if (s != FP8_OK) return s;
         s = make_scale_map<KB>(&tmSB, g.sfb, g.N, g.sfb_ld, kBnPair);
         if (s != FP8_OK) return s;
+        CUtensorMap tmD;  // D is 16-byte aligned with 16-byte aligned rows (checked by the API)
+        s = make_out_map(&tmD, g.D, g.M, g.N, g.ldd, OUT_BF16 != 0);
+        if (s != FP8_OK) return s;
         auto kp = gemm_blockscaled_pair_kernel<OUT_BF16, KA, KB>;
         const size_t smem_p = sizeof(SmemBsPair) + 1024;
         s = prepare_kernel(reinterpret_cast<const void*>(kp), smem_p);
         if (s != FP8_OK) return s;
-        return launch_pair_kernel(kp, smem_p, 320, st, tmA, tmB, tmSA, tmSB, g, idesc);
+        return launch_pair_kernel(kp, smem_p, 320, st, tmA, tmB, tmSA, tmSB, tmD, g, idesc);
     }
     const size_t smem = sizeof(SmemBS) + 1024;
     auto k = gemm_blockscaled_kernel<OUT_BF16, KA, KB>;

@@ -235,6 +235,30 @@ def test_gemm_block_pair_ragged_last_column(q, w, ga, gb):
 
 
 @pytest.mark.parametrize("out_bf16", [False, True])
+@pytest.mark.parametrize("offset", [0, 16])
+def test_gemm_block_pair_output_pitch_and_offset(q, out_bf16, offset):
+    """The CTA-pair block-scaled kernel, whose epilogue writes D with TMA stores of 32 x 32 boxes,
+    into a strided D (ldd = N + 64) starting `offset` columns into each padded row, with ragged edges
+    (M = 520, N = 784: partial boxes in both directions).  Values match the oracle, and nothing
+    outside the N columns of D is written."""
+    rng = np.random.default_rng(80 + offset + out_bf16)
+    M, N, K = 520, 784, 1024
+    A, B = realistic_codes(rng, (M, K), 0), realistic_codes(rng, (N, K), 0)
+    sfa, sfb = mx_scales(rng, M, K), mx_scales(rng, N, K)
+    dt = torch.bfloat16 if out_bf16 else torch.float32
+    Dfull = torch.zeros(M, N + 64, dtype=dt, device="cuda")
+    D = Dfull[:, offset:offset + N]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q.fp8_scaled_gemm(0, _dev(A), 0, q.MX_1x32, _dev(sfa), _dev(B), 0, q.MX_1x32, _dev(sfb), D, status=status)
+    y = bf16_out_to_f64(D) if out_bf16 else host(D).astype(np.float64)
+    assert int(host(status)[0]) == 0
+    y_ref, mag = oracle.gemm_full(A, 0, 3, sfa, B, 0, 3, sfb)
+    assert_gemm_close(y, y_ref, mag, out_bf16)
+    full = host(Dfull.float() if out_bf16 else Dfull)
+    assert not full[:, :offset].any() and not full[:, offset + N:].any(), "wrote outside D"
+
+
+@pytest.mark.parametrize("out_bf16", [False, True])
 def test_gemm_nan_operand_poisons_its_row_only(q, out_bf16):
     """A NaN code in A makes its output row NaN (the fp64 oracle agrees); every other row is finite
     and within tolerance."""
