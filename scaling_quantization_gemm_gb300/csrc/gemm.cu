@@ -166,6 +166,79 @@ __device__ __forceinline__ void store_out(const GemmArgs& g, int64_t row, int64_
         store_row32<OUT>(g, row, col0, r, sa, sb);
 }
 
+// Epilogue through TMA stores.  Each epilogue warp owns a 4 KB staging buffer in shared memory; a
+// 32-row x 32-column output chunk (row `lane` from each lane) is written into it in the swizzle of the
+// output tensor map (fp32 rows of 128 bytes: 128-byte swizzle; bf16, 64 bytes: 64-byte swizzle; FP8,
+// 32 bytes: 32-byte swizzle -- 16-byte chunk j of row r at j ^ (r % 8), j ^ (r / 2 % 4), j ^ (r / 4 % 2),
+// which puts a warp's 16-byte stores in distinct bank groups), then one thread issues one
+// cp.async.bulk.tensor store of the chunk, which the tensor map clips at the edges of D.  Chunks
+// rotate through the buffer's 4096 / chunk-bytes slots; before a slot is reused the store that last
+// read it must be done reading (cp.async.bulk.wait_group.read).
+constexpr int kOutStageBytes = 4096;
+template <int OUT>
+__host__ __device__ constexpr int out_chunk_bytes() { return OUT == 0 ? 4096 : OUT == 1 ? 2048 : 1024; }
+template <int OUT>
+__host__ __device__ constexpr int out_slots() { return kOutStageBytes / out_chunk_bytes<OUT>(); }
+
+// Stage row `lane` of a chunk: values v = (acc sa) sb (SCALED) or acc; FP8 outputs hold the codes of
+// v sd, and fold max |v| into `amax` (as bits, so a NaN wins).
+template <int OUT, bool SCALED>
+__device__ __forceinline__ void stage_out_row(uint32_t slot, int lane, const uint32_t (&r)[32], float sa, float sb,
+                                              float sd, uint32_t& amax) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = SCALED ? __fmul_rn(__fmul_rn(__uint_as_float(r[i]), sa), sb) : __uint_as_float(r[i]);
+    if constexpr (OUT == 0) {
+        const uint32_t line = slot + (uint32_t)lane * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(line + ((uint32_t)(j ^ (lane & 7)) << 4), __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                         __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+    } else if constexpr (OUT == 1) {
+        const uint32_t line = slot + (uint32_t)lane * 64u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            st_shared_v4(line + ((uint32_t)(j ^ ((lane >> 1) & 3)) << 4), cvt_bf16x2(v[8 * j], v[8 * j + 1]),
+                         cvt_bf16x2(v[8 * j + 2], v[8 * j + 3]), cvt_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                         cvt_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+    } else {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            amax = max(amax, max(__float_as_uint(v[2 * i]) & 0x7FFFFFFFu, __float_as_uint(v[2 * i + 1]) & 0x7FFFFFFFu));
+            const uint32_t c = cvt_fp8x2<OUT - 2>(__fmul_rn(v[2 * i], sd), __fmul_rn(v[2 * i + 1], sd));
+            if (i & 1)
+                w[i >> 1] |= c << 16;
+            else
+                w[i >> 1] = c;
+        }
+        const uint32_t line = slot + (uint32_t)lane * 32u;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            st_shared_v4(line + ((uint32_t)(j ^ ((lane >> 2) & 1)) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    }
+}
+
+// One chunk through the warp's staging buffer: `nchunk` counts the warp's chunks (slot rotation).
+// Rows row0 .. row0 + 31 of D, columns col0 .. col0 + 31; nothing is stored when all lie outside D.
+template <int OUT, bool SCALED>
+__device__ __forceinline__ void store_chunk_tma(const CUtensorMap* tmD, uint32_t buf, uint32_t& nchunk, int lane,
+                                                const uint32_t (&r)[32], float sa, float sb, float sd, uint32_t& amax,
+                                                int64_t row0, int64_t col0, const GemmArgs& g) {
+    const uint32_t slot = buf + (nchunk % (uint32_t)out_slots<OUT>()) * (uint32_t)out_chunk_bytes<OUT>();
+    ++nchunk;
+    if (lane == 0) bulk_wait_read<out_slots<OUT>() - 1>();  // the store that last read `slot` is done reading
+    __syncwarp();
+    stage_out_row<OUT, SCALED>(slot, lane, r, sa, sb, sd, amax);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (row0 < g.M && col0 < g.N) tma_store_2d(tmD, slot, (int)col0, (int)row0);
+        bulk_commit();
+    }
+}
+
 // End of an epilogue warp: fold the warp's amax into the caller's accumulator.
 template <int OUT>
 __device__ __forceinline__ void flush_amax(const GemmArgs& g, uint32_t amax) {
@@ -362,6 +435,7 @@ constexpr int kPairStageBytes = 2 * kPairHalfBytes; // A half + B half, per CTA
 struct alignas(1024) SmemPair {
     uint8_t a[kPairStages][kPairHalfBytes];
     uint8_t b[kPairStages][kPairHalfBytes];
+    alignas(1024) uint8_t out[4][kOutStageBytes];  // per epilogue warp: staged output chunks for TMA stores
     uint64_t full[kPairStages], empty[kPairStages], tfull[2], tempty[2], drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -369,8 +443,8 @@ struct alignas(1024) SmemPair {
 
 template <int OUT>
 __global__ void __launch_bounds__(192, 1)
-    gemm_tensor_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g,
-                            uint32_t idesc) {
+    gemm_tensor_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmD, GemmArgs g, uint32_t idesc) {
     extern __shared__ uint8_t smem_raw[];
     SmemPair& S = *reinterpret_cast<SmemPair*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -392,6 +466,7 @@ __global__ void __launch_bounds__(192, 1)
         mbar_fence_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmD);
     }
     cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
     if (warp == 1) {
@@ -475,6 +550,8 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t amax = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
+        const uint32_t obuf = smem_u32(S.out[q]);
+        uint32_t nchunk = 0;  // chunks this warp has staged
         for (int t = cid; t < g.num_tiles; t += ncl) {
             bool ok = mbar_wait_bounded(smem_u32(&S.tfull[acc]), acc_phase, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
@@ -482,14 +559,14 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after();
             int tm, tn;
             tile_coords(t, g, tm, tn);
-            const int64_t row = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows + q * 32 + lane;
+            const int64_t row0 = (int64_t)tm * kPairTile + (int64_t)rank * kPairRows + q * 32;  // this warp's rows
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
                 const int64_t col0 = (int64_t)tn * kPairTile + c * 32;
-                if (row < g.M) store_out<OUT>(g, row, col0, r, sa, sb, sd, amax);
+                store_chunk_tma<OUT, true>(&tmD, obuf, nchunk, lane, r, sa, sb, sd, amax, row0, col0, g);
             }
             tc_fence_before();
             __syncwarp();
@@ -497,6 +574,7 @@ __global__ void __launch_bounds__(192, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
+        if (lane == 0) bulk_wait_all();  // this warp's stores are complete before the CTA exits
         flush_amax<OUT>(g, amax);
     }
 
@@ -801,10 +879,7 @@ constexpr int kBsPairStageBytes = kBsKPerStage * (kBsPairABytes + kBsPairBBytes)
 constexpr int kScaleSlots = 4;
 constexpr int kScaleAhead = 2;  // scale groups loaded ahead of the group being consumed
 constexpr int kScaleBlockRowsB = 3;                    // a tile's B rows touch at most three 128-row blocks
-// Epilogue staging for TMA stores of D: per warp 32 rows x 32 columns, as two 2 KB halves for bf16
-// (alternating chunks) or one 4 KB buffer for fp32; rows in the 64-byte (bf16) or 128-byte (fp32)
-// swizzle of the store's tensor map.
-constexpr int kOutStageBytes = 4096;
+
 static_assert(kBnPair <= 2 * 128 + 1, "a tile's B rows span at most three 128-row blocks");
 
 struct alignas(1024) SmemBsPair {
@@ -1067,7 +1142,7 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t acc_phase = 0;
         bool bad = false;
         const uint32_t obuf = smem_u32(S.out[q]);
-        uint32_t nchunk = 0;  // chunks this warp has staged (bf16 alternates the two halves of its buffer)
+        uint32_t nchunk = 0;  // chunks this warp has staged
         for (int t = cid; t < g.num_tiles; t += ncl) {
             int tm, tn;
             tile_coords(t, g, tm, tn);
@@ -1084,35 +1159,8 @@ __global__ void __launch_bounds__(320, 1)
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
                 const int64_t col0 = (int64_t)tn * kBnPair + c * 32;
-                {
-                    // stage row `lane` of the 32 x 32 chunk, then one TMA store per warp (clipped at the edges)
-                    const uint32_t buf = obuf + (OUT_BF16 ? (nchunk & 1u) * 2048u : 0u);
-                    ++nchunk;
-                    if (lane == 0) bulk_wait_read<OUT_BF16 ? 1 : 0>();  // the store that last read `buf` is done
-                    __syncwarp();
-                    if constexpr (OUT_BF16) {
-                        const uint32_t line = buf + (uint32_t)lane * 64u;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            st_shared_v4(line + ((uint32_t)(j ^ ((lane >> 1) & 3)) << 4),
-                                         cvt_bf16x2(__uint_as_float(r[8 * j]), __uint_as_float(r[8 * j + 1])),
-                                         cvt_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
-                                         cvt_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
-                                         cvt_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
-                    } else {
-                        const uint32_t line = buf + (uint32_t)lane * 128u;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            st_shared_v4(line + ((uint32_t)(j ^ (lane & 7)) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2],
-                                         r[4 * j + 3]);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (row0 < g.M && col0 < g.N) tma_store_2d(&tmD, buf, (int)col0, (int)row0);
-                        bulk_commit();
-                    }
-                }
+                uint32_t unused_amax = 0;
+                store_chunk_tma<OUT_BF16, false>(&tmD, obuf, nchunk, lane, r, 1.0f, 1.0f, 1.0f, unused_amax, row0, col0, g);
             }
             tc_fence_before();
             __syncwarp();
@@ -1236,18 +1284,24 @@ fp8_status make_operand_map(CUtensorMap* map, const void* ptr, int64_t rows, int
     return FP8_OK;
 }
 
-// 2-D map over the output D [M x N] (row pitch ldd elements) for the pair epilogue's TMA stores: box 32 x 32,
-// rows of the box in the 64-byte (bf16) or 128-byte (fp32) swizzle.
-fp8_status make_out_map(CUtensorMap* map, void* ptr, int64_t M, int64_t N, int64_t ldd, bool bf16) {
+// 2-D map over the output D [M x N] (row pitch ldd elements) of output kind `out` (0 fp32, 1 bf16, 2/3
+// FP8) for the pair epilogues' TMA stores: box 32 x 32, rows of the box in the swizzle whose span is
+// the box row (128, 64 or 32 bytes), as the epilogue stages them.
+fp8_status make_out_map(CUtensorMap* map, void* ptr, int64_t M, int64_t N, int64_t ldd, int out) {
     auto fn = encode_fn();
     FP8_REQUIRE(fn != nullptr, FP8_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-    const int64_t es = bf16 ? 2 : 4;
+    const int64_t es = out == 0 ? 4 : out == 1 ? 2 : 1;
     cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)(ldd * es)};
     cuuint32_t box[2] = {32, 32};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+    const CUtensorMapDataType dt = out == 0   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : out == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const CUtensorMapSwizzle sw = out == 0   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : out == 1 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_32B;
+    CUresult r = fn(map, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     FP8_REQUIRE(r == CUDA_SUCCESS, FP8_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", (int)r);
     return FP8_OK;
@@ -1336,9 +1390,12 @@ fp8_status launch_pair_kernel(Kernel k, size_t smem, int threads, cudaStream_t s
 template <int OUT>
 fp8_status launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g, uint32_t idesc,
                        cudaStream_t st) {
-    fp8_status s = prepare_kernel(reinterpret_cast<const void*>(gemm_tensor_pair_kernel<OUT>), sizeof(SmemPair) + 1024);
+    CUtensorMap tmD;  // D is 16-byte aligned with 16-byte aligned rows (checked by the API)
+    fp8_status s = make_out_map(&tmD, g.D, g.M, g.N, g.ldd, OUT);
     if (s != FP8_OK) return s;
-    return launch_pair_kernel(gemm_tensor_pair_kernel<OUT>, sizeof(SmemPair) + 1024, 192, st, tmA, tmB, g, idesc);
+    s = prepare_kernel(reinterpret_cast<const void*>(gemm_tensor_pair_kernel<OUT>), sizeof(SmemPair) + 1024);
+    if (s != FP8_OK) return s;
+    return launch_pair_kernel(gemm_tensor_pair_kernel<OUT>, sizeof(SmemPair) + 1024, 192, st, tmA, tmB, tmD, g, idesc);
 }
 
 template <int OUT>
@@ -1364,7 +1421,7 @@ fp8_status launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmA
         s = make_scale_map<KB>(&tmSB, g.sfb, g.N, g.sfb_ld, kBnPair);
         if (s != FP8_OK) return s;
         CUtensorMap tmD;  // D is 16-byte aligned with 16-byte aligned rows (checked by the API)
-        s = make_out_map(&tmD, g.D, g.M, g.N, g.ldd, OUT_BF16 != 0);
+        s = make_out_map(&tmD, g.D, g.M, g.N, g.ldd, OUT_BF16);
         if (s != FP8_OK) return s;
         auto kp = gemm_blockscaled_pair_kernel<OUT_BF16, KA, KB>;
         const size_t smem_p = sizeof(SmemBsPair) + 1024;
