@@ -13,8 +13,9 @@
 //               128-wide K tile is four K=32 MMAs.
 //   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), unscale, convert
 //               (fp32, bf16, or E4M3/E5M2 with a given scale and a fused amax),
-//               store.  Each warp owns the 32 TMEM lanes (= tile rows) that its
-//               warp index selects.
+//               store (the pair kernels stage 32x32 chunks in shared memory and
+//               store them with TMA).  Each warp owns the 32 TMEM lanes (= tile
+//               rows) that its warp index selects.
 //   warps 6-9   (block-scaled kernels only) scale-factor writers.
 // Two fp32 accumulators live in TMEM so the epilogue of one tile overlaps the
 // main loop of the next.  M > 128 runs on CTA pairs (clusters of two, tcgen05
@@ -65,9 +66,9 @@ static_assert(kSfbCols <= 8, "B scales of a tile fill at most eight TMEM columns
 
 // Block-scaled CTA-pair kernel: pair tile width and TMEM layout (accumulators, then scale slots).
 // Measured on the MXFP8 and per-block shapes: 224 columns with two accumulators beat 192 with eight
-// scale slots and 256 with one accumulator (the block-scaled MMAs cost about the same per stage
-// beyond their arithmetic whatever the width, so narrower tiles lose and one accumulator exposes the
-// epilogue).
+// scale slots and 256 with one accumulator (a stage costs about the same beyond its arithmetic
+// whatever the width -- the tensor core waits on the kernel's other traffic, not on the MMA -- so
+// narrower tiles lose, and one accumulator exposes the epilogue).
 constexpr int kBnPair = 224;   // output columns (B rows) of a pair tile
 constexpr int kAccBufs = 2;    // accumulators: with two, a tile's epilogue overlaps the next tile's MMAs
 constexpr int kSfColBasePair = kAccBufs * kBnPair;
@@ -440,6 +441,8 @@ struct alignas(1024) SmemPair {
     uint32_t tmem_base;
     int abort_flag;
 };
+
+static_assert(sizeof(SmemPair) + 1024 <= 232448, "the pair kernel's shared memory fits one SM (227 KB)");
 
 template <int OUT>
 __global__ void __launch_bounds__(192, 1)
