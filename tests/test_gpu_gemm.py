@@ -258,6 +258,36 @@ def test_gemm_block_pair_output_pitch_and_offset(q, out_bf16, offset):
     assert not full[:, :offset].any() and not full[:, offset + N:].any(), "wrote outside D"
 
 
+@pytest.mark.parametrize("M,N", [(129, 16), (384, 48), (136, 1008), (257, 32)])
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_gemm_pair_epilogue_edges(q, M, N, out_bf16):
+    """The CTA-pair kernels' TMA-store epilogue at its edges: N narrower than one 32-column box (16) or
+    not a multiple of 32, and M just past one 256-row pair tile (129, 257: the second CTA of the last
+    pair, or all of its rows but one, outside D), per-tensor and MX, fp32 and bf16 out.  D matches
+    the oracle and nothing past the N columns of each row is touched."""
+    rng = np.random.default_rng(M * 7 + N + out_bf16)
+    K = 512
+    A, B = realistic_codes(rng, (M, K), 0), realistic_codes(rng, (N, K), 0)
+    dt = torch.bfloat16 if out_bf16 else torch.float32
+    for gran in (0, q.MX_1x32):
+        Dfull = torch.full((M, N + 32), 7.0, dtype=dt, device="cuda")
+        D = Dfull[:, :N]
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if gran == 0:
+            sa, sb = np.float32(0.5), np.float32(0.25)
+            q.fp8_scaled_gemm(0, _dev(A), 0, 0, torch.tensor([sa], device="cuda"), _dev(B), 0, 0,
+                              torch.tensor([sb], device="cuda"), D, status=status)
+            y_ref, mag = oracle.gemm_full(A, 0, 0, sa, B, 0, 0, sb)
+        else:
+            sfa, sfb = mx_scales(rng, M, K), mx_scales(rng, N, K)
+            q.fp8_scaled_gemm(0, _dev(A), 0, gran, _dev(sfa), _dev(B), 0, gran, _dev(sfb), D, status=status)
+            y_ref, mag = oracle.gemm_full(A, 0, 3, sfa, B, 0, 3, sfb)
+        assert int(host(status)[0]) == 0
+        y = bf16_out_to_f64(D) if out_bf16 else host(D).astype(np.float64)
+        assert_gemm_close(y, y_ref, mag, out_bf16)
+        assert (host(Dfull.float())[:, N:] == 7.0).all(), "wrote past N"
+
+
 @pytest.mark.parametrize("out_bf16", [False, True])
 def test_gemm_nan_operand_poisons_its_row_only(q, out_bf16):
     """A NaN code in A makes its output row NaN (the fp64 oracle agrees); every other row is finite

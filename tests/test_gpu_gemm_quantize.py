@@ -60,7 +60,8 @@ def delayed_like_scale(y_ref, fd):
     return float(oracle.scale_triple(np.float32(np.abs(y_ref).max()), fd)[1])
 
 
-SHAPES = [(128, 256, 256), (200, 272, 384), (512, 512, 1024), (96, 48, 128), (384, 16, 64)]
+SHAPES = [(128, 256, 256), (200, 272, 384), (512, 512, 1024), (96, 48, 128), (384, 16, 64), (129, 48, 512),
+          (257, 1008, 512)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
