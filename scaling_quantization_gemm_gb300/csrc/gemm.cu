@@ -845,9 +845,9 @@ __global__ void __launch_bounds__(320, 1)
 // scales of its own A rows and of all 224 B rows from its own TMEM, so both
 // CTAs' scale writers fill their own scale slots (A row m: lane m, column m/32;
 // B row n: lane 32q + n%32, column 8 + n/32, every quarter q).  The producer
-// TMA-loads the scales of each group of four K tiles (16 bytes per row: the A
-// rows of this CTA and all B rows of the tile) into a four-slot shared-memory
-// ring, two groups ahead.  When a group lands, each writer thread reads the
+// TMA-loads the scales of each pair of groups of four K tiles (32 bytes per
+// row: the A rows of this CTA and all B rows of the tile) into a two-slot
+// shared-memory ring, one slot ahead.  When a group lands, each writer thread reads the
 // words of its rows for the group's four K tiles into registers -- E8M0 words
 // as they are; power-of-two fp32 block scales (1x128, 128x128) re-encoded as
 // E8M0 and repeated over the four 32-wide sub-blocks -- and frees the slot, so
@@ -879,8 +879,11 @@ constexpr int kBsPairB = kBnPair / 2;                    // rows of B per CTA
 constexpr int kBsPairABytes = kPairRows * BK;          // 16 KB per K tile
 constexpr int kBsPairBBytes = kBsPairB * BK;           // B bytes per K tile and CTA
 constexpr int kBsPairStageBytes = kBsKPerStage * (kBsPairABytes + kBsPairBBytes);
-constexpr int kScaleSlots = 4;
-constexpr int kScaleAhead = 2;  // scale groups loaded ahead of the group being consumed
+// Scale ring: each slot holds the scales of two groups of four K tiles (32 bytes per row), so a TMA
+// box of 128 (A) or 224 (B) rows carries twice the bytes per row request; two slots.
+constexpr int kScaleGroupsPerSlot = 2;
+constexpr int kScaleRowBytes = 16 * kScaleGroupsPerSlot;
+constexpr int kScaleSlots = 2;
 constexpr int kScaleBlockRowsB = 3;                    // a tile's B rows touch at most three 128-row blocks
 
 static_assert(kBnPair <= 2 * 128 + 1, "a tile's B rows span at most three 128-row blocks");
@@ -888,8 +891,8 @@ static_assert(kBnPair <= 2 * 128 + 1, "a tile's B rows span at most three 128-ro
 struct alignas(1024) SmemBsPair {
     uint8_t a[kBsPairStages][kBsKPerStage * kBsPairABytes];
     uint8_t b[kBsPairStages][kBsKPerStage * kBsPairBBytes];
-    alignas(128) uint8_t sa[kScaleSlots][kPairRows * 16];  // per row: four K tiles x 4 bytes (E8M0 x4 or one fp32)
-    alignas(128) uint8_t sb[kScaleSlots][kBnPair * 16];
+    alignas(128) uint8_t sa[kScaleSlots][kPairRows * kScaleRowBytes];  // per row and group: four K tiles x 4 bytes
+    alignas(128) uint8_t sb[kScaleSlots][kBnPair * kScaleRowBytes];
     alignas(1024) uint8_t out[4][kOutStageBytes];  // per epilogue warp: staged output chunks for TMA stores
     uint64_t full[kBsPairStages], empty[kBsPairStages], tfull[2], tempty[2], drain;
     uint64_t scale_full[kScaleSlots], scale_empty[kScaleSlots];
@@ -934,14 +937,14 @@ __device__ __forceinline__ uint32_t e8m0_code(uint32_t raw) {
 // are, fp32 block scales as their E8M0 code.  Local row r of the slot, or for 128x128 scales the
 // block row of `row` counted from `block_base`; rows past the edge get the neutral scale 1.
 template <int KIND>
-__device__ __forceinline__ void sf_group_words(const uint8_t* slot, int r, int block_base, int64_t row, int64_t rows,
-                                               uint32_t (&w)[4]) {
+__device__ __forceinline__ void sf_group_words(const uint8_t* slot, int half, int r, int block_base, int64_t row,
+                                               int64_t rows, uint32_t (&w)[4]) {
     if (row >= rows) {
         w[0] = w[1] = w[2] = w[3] = 0x7F7F7F7Fu;
         return;
     }
     const int sr = KIND == SF_BLOCK ? (int)(row >> 7) - block_base : r;
-    const uint4 v = *reinterpret_cast<const uint4*>(slot + sr * 16);
+    const uint4 v = *reinterpret_cast<const uint4*>(slot + sr * kScaleRowBytes + half * 16);
     const uint32_t raw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) w[jj] = KIND == SF_MX ? raw[jj] : e8m0_code(raw[jj]) * 0x01010101u;
@@ -998,8 +1001,9 @@ __global__ void __launch_bounds__(320, 1)
     const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
     const int groups = (g.k_tiles + 3) / 4;
     volatile int* abort_flag = &S.abort_flag;
-    constexpr int kSaBytes = scale_box_rows<KA>(kPairRows) * 16;
-    constexpr int kSbBytes = scale_box_rows<KB>(kBnPair) * 16;
+    constexpr int kSaBytes = scale_box_rows<KA>(kPairRows) * kScaleRowBytes;
+    constexpr int kSbBytes = scale_box_rows<KB>(kBnPair) * kScaleRowBytes;
+    const int pairs = (groups + kScaleGroupsPerSlot - 1) / kScaleGroupsPerSlot;  // scale slots per tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBsPairStages; ++s) {
@@ -1039,8 +1043,8 @@ __global__ void __launch_bounds__(320, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            int issued = 0;                    // scale groups issued so far (flattened over this pair's tiles)
-            int nt = cid, ngrp = 0;            // the next (tile, group) whose scales to load
+            int issued = 0;                    // scale slots issued so far (flattened over this pair's tiles)
+            int nt = cid, npair = 0;           // the next (tile, pair of groups) whose scales to load
             auto issue_next_scales = [&]() -> bool {
                 if (nt >= g.num_tiles || groups == 0) return true;
                 const int slot = issued % kScaleSlots;
@@ -1050,24 +1054,26 @@ __global__ void __launch_bounds__(320, 1)
                     return false;
                 int tm, tn;
                 tile_coords(nt, g, tm, tn);
-                const int xa = KA == SF_MX ? 16 * ngrp : 4 * ngrp, xb = KB == SF_MX ? 16 * ngrp : 4 * ngrp;
+                const int xa = (KA == SF_MX ? 16 : 4) * kScaleGroupsPerSlot * npair;
+                const int xb = (KB == SF_MX ? 16 : 4) * kScaleGroupsPerSlot * npair;
                 const int arow = tm * kPairTile + (int)rank * kPairRows, brow = tn * kBnPair;
                 mbar_arrive_expect_tx(smem_u32(&S.scale_full[slot]), kSaBytes + kSbBytes);
                 tma_load_2d(smem_u32(S.sa[slot]), &tmSA, smem_u32(&S.scale_full[slot]), xa, KA == SF_BLOCK ? arow >> 7 : arow);
                 tma_load_2d(smem_u32(S.sb[slot]), &tmSB, smem_u32(&S.scale_full[slot]), xb, KB == SF_BLOCK ? brow >> 7 : brow);
                 ++issued;
-                if (++ngrp == groups) {
-                    ngrp = 0;
+                if (++npair == pairs) {
+                    npair = 0;
                     nt += ncl;
                 }
                 return true;
             };
-            for (int i = 0; ok && i < kScaleAhead; ++i) ok = issue_next_scales();
+            ok = issue_next_scales();  // one slot ahead of the slot being consumed
             for (int t = cid; ok && t < g.num_tiles; t += ncl) {
                 int tm, tn;
                 tile_coords(t, g, tm, tn);
                 for (int kt = 0; kt < g.k_tiles; kt += kBsKPerStage) {  // k_tiles is a multiple of 4 here
-                    if ((kt & 3) == 0 && !(ok = issue_next_scales())) break;  // entering a group: keep two ahead
+                    // entering a slot's first group: load the next slot
+                    if ((kt % (4 * kScaleGroupsPerSlot)) == 0 && !(ok = issue_next_scales())) break;
                     if (!mbar_wait_bounded(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag)) {
                         ok = false;
                         break;
@@ -1194,22 +1200,27 @@ __global__ void __launch_bounds__(320, 1)
             const int ablock = (tm * kPairTile + (int)rank * kPairRows) >> 7;
             const int bblock = (tn * kBnPair) >> 7;
             for (int grp = 0; ok && grp < groups; ++grp) {  // k_tiles is a multiple of 4 on this path
-                const int slot = consumed % kScaleSlots;
-                bool w = mbar_wait_bounded(smem_u32(&S.scale_full[slot]), (uint32_t)((consumed / kScaleSlots) & 1),
-                                           abort_flag);
-                if (!__all_sync(0xffffffffu, w)) {
-                    ok = false;
-                    break;
+                const int slot = consumed % kScaleSlots, half = grp % kScaleGroupsPerSlot;
+                bool w = true;
+                if (half == 0) {
+                    w = mbar_wait_bounded(smem_u32(&S.scale_full[slot]), (uint32_t)((consumed / kScaleSlots) & 1),
+                                          abort_flag);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 uint32_t wa[4], wb[kSfbColsPair][4];
-                sf_group_words<KA>(S.sa[slot], q * 32 + lane, ablock, arow, g.M, wa);
+                sf_group_words<KA>(S.sa[slot], half, q * 32 + lane, ablock, arow, g.M, wa);
 #pragma unroll
                 for (int j = 0; j < kSfbColsPair; ++j)
-                    sf_group_words<KB>(S.sb[slot], 32 * j + lane, bblock, (int64_t)tn * kBnPair + 32 * j + lane, g.N,
-                                       wb[j]);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&S.scale_empty[slot]));  // the producer may refill the slot
-                ++consumed;
+                    sf_group_words<KB>(S.sb[slot], half, 32 * j + lane, bblock, (int64_t)tn * kBnPair + 32 * j + lane,
+                                       g.N, wb[j]);
+                if (half == kScaleGroupsPerSlot - 1 || grp == groups - 1) {  // the slot's last group of this tile
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&S.scale_empty[slot]));  // the producer may refill the slot
+                    ++consumed;
+                }
 #pragma unroll
                 for (int u = 0; u < 4 / kBsKPerStage; ++u) {  // one stage (two K tiles) per arrival
                     if (kcount >= kSfAhead * kBsKPerStage) {
@@ -1330,8 +1341,8 @@ int pair_tiles_of(const GemmArgs& g, const Rest&...) { return g.num_tiles; }
 template <typename T, typename... Rest>
 int pair_tiles_of(const T&, const Rest&... rest) { return pair_tiles_of(rest...); }
 
-// 2-D map over a scale tensor for one group of four K tiles per row: 16 bytes per row (four E8M0
-// words' bytes, or four fp32), `box_rows` rows (or 128-row blocks for 128x128 scales).
+// 2-D map over a scale tensor for two groups of four K tiles per row: 32 bytes per row (eight E8M0
+// words' bytes, or eight fp32), `box_rows` rows (or 128-row blocks for 128x128 scales).
 template <int KIND>
 fp8_status make_scale_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t ld, int tile_rows) {
     auto fn = encode_fn();
@@ -1340,7 +1351,7 @@ fp8_status make_scale_map(CUtensorMap* map, const void* ptr, int64_t rows, int64
     const int64_t srows = KIND == SF_BLOCK ? (rows + 127) / 128 : rows;
     cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)srows};
     cuuint64_t strides[1] = {(cuuint64_t)(mx ? ld : 4 * ld)};
-    cuuint32_t box[2] = {(cuuint32_t)(mx ? 16 : 4), (cuuint32_t)scale_box_rows<KIND>(tile_rows)};
+    cuuint32_t box[2] = {(cuuint32_t)((mx ? 16 : 4) * kScaleGroupsPerSlot), (cuuint32_t)scale_box_rows<KIND>(tile_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr),
                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

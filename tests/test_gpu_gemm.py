@@ -126,7 +126,7 @@ def pow2_scales(rng, shape):
 
 
 BS_SHAPES = [(128, 256, 128), (256, 512, 512), (200, 272, 384), (384, 1024, 1024), (128, 256, 2048),
-             (520, 784, 2048)]
+             (520, 784, 2048), (384, 480, 1536)]
 
 
 @pytest.mark.parametrize("M,N,K", BS_SHAPES)
