@@ -118,3 +118,97 @@ def test_writers_bounded_by_the_slot_ring_alone_break_the_operand_ring():
         except AssertionError:
             failures += 1
     assert failures > 50
+
+
+# ------------------------------------------------------------------ scale ring
+
+def ring_constants():
+    src = open(GEMM).read()
+    return {"slots": _const(src, "kScaleSlots"), "per_slot": _const(src, "kScaleGroupsPerSlot")}
+
+
+def simulate_scale_ring(slots, per_slot, groups, tiles, seed, release_each_group=False):
+    """The producer loads the scales of `per_slot` groups of one tile per ring slot, one slot ahead: the
+    first at start-up, then one each time its operand loop enters a slot's first group; it waits for
+    the slot's previous contents to have been consumed (`scale_empty`, parity of the refill).  Each of
+    four writer warps waits for the slot (`scale_full`, parity) at a slot's first group, reads a group's
+    words, and releases the slot after its last group of that tile.  Checks that every group's words
+    come from the load of its own (tile, group), that no slot is refilled before all four writers
+    released it, that no parity wait laps its barrier, and that nothing deadlocks."""
+    rnd = random.Random(seed)
+    pairs = -(-groups // per_slot)
+    order = [(t, p) for t in range(tiles) for p in range(pairs)]  # slot loads in issue order
+    full = [Barrier(1) for _ in range(slots)]
+    empty = [Barrier(4) for _ in range(slots)]
+    content = [None] * slots
+    readers = [0] * slots  # writers yet to release the slot's current contents
+    issued = 0
+    prod_pos = 0            # the producer's position: groups entered so far (flattened)
+    flat = [(t, g) for t in range(tiles) for g in range(groups)]
+    wpos = [0] * 4          # each writer's next flattened group
+    wcons = [0] * 4         # slots each writer has consumed
+
+    def issue():
+        nonlocal issued
+        if issued >= len(order):
+            return True
+        s = issued % slots
+        if issued >= slots and not empty[s].completed(issued // slots - 1):
+            return False
+        assert readers[s] == 0, "a slot was refilled before its writers released it"
+        content[s] = order[issued]
+        readers[s] = 4
+        full[s].arrive()
+        issued += 1
+        return True
+
+    assert issue()
+    for _ in range(200000):
+        if all(p == len(flat) for p in wpos) and prod_pos == len(flat):
+            return
+        acts = []
+        if prod_pos < len(flat):
+            acts.append(("p", 0))
+        for w in range(4):
+            if wpos[w] < len(flat):
+                t, gr = flat[wpos[w]]
+                s = wcons[w] % slots
+                if gr % per_slot != 0 or full[s].completed(wcons[w] // slots):
+                    acts.append(("w", w))
+        assert acts, "deadlock"
+        kind, i = rnd.choice(acts)
+        if kind == "p":
+            t, gr = flat[prod_pos]
+            if gr % per_slot == 0:
+                if not issue():
+                    continue  # waiting for a slot to be released
+            prod_pos += 1
+        else:
+            t, gr = flat[wpos[i]]
+            s = wcons[i] % slots
+            assert content[s] == (t, gr // per_slot), "a writer read another tile's or group's scales"
+            wpos[i] += 1
+            if release_each_group or gr % per_slot == per_slot - 1 or gr == groups - 1:
+                readers[s] -= 1
+                empty[s].arrive()
+                wcons[i] += 1
+    raise AssertionError("deadlock")
+
+
+@pytest.mark.parametrize("groups", [1, 2, 3, 4, 5])
+def test_scale_ring_under_random_schedules(groups):
+    k = ring_constants()
+    for seed in range(60):
+        simulate_scale_ring(k["slots"], k["per_slot"], groups, 5, seed)
+
+
+def test_scale_ring_releasing_each_group_breaks():
+    """Writers that release a two-group slot after each group let the producer refill it (or the
+    barrier run ahead) while its second group is still to be read."""
+    failures = 0
+    for seed in range(60):
+        try:
+            simulate_scale_ring(2, 2, 4, 5, seed, release_each_group=True)
+        except AssertionError:
+            failures += 1
+    assert failures > 30
