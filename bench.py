@@ -306,6 +306,9 @@ def run_ours(args, rank, world):
     b_ev.record(stream)
     torch.cuda.synchronize()
     power_cap["ms_per_step_without_op_events"] = round(max_over_ranks(a_ev.elapsed_time(b_ev), world) / args.steps, 3)
+    # the same step for about a second: NVML's clock reading lags by tens of ms, so a short timed region
+    # is mostly sampled before the cap bites; this record shows the clock once it has
+    power_cap["sustained"] = sustained_load(ops, stream, ms_step, dev.index, world)
     status = [int(c4.status.item()), int(c3.status.item())] + [int(s.status.item()) for s in (c5.sx, c5.sw, c5.sg)]
 
     # --- end to end: pinned host inputs in, results out, every step ---
@@ -371,6 +374,35 @@ def run_ours(args, rank, world):
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def sustained_load(ops, stream, ms_step: float, gpu_index: int, world: int, seconds: float = 1.0) -> dict:
+    """The step repeated for about `seconds` with the clock sampler on (not part of the timed region):
+    steps, mean ms per step, the clock record, and each op's mean time over the last five steps."""
+    import torch
+    n = max(20, int(seconds * 1000.0 / max(ms_step, 1e-3)))
+    tail = 5
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(tail)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as sampler:
+        a.record(stream)
+        for k in range(n):
+            t = k - (n - tail)
+            if t >= 0:
+                evs[t][0].record(stream)
+            for i, (_, f, *_) in enumerate(ops):
+                f()
+                if t >= 0:
+                    evs[t][i + 1].record(stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+    total = max_over_ranks(a.elapsed_time(b), world)
+    last = {ops[i][0]: round(statistics.mean(evs[t][i].elapsed_time(evs[t][i + 1]) for t in range(tail)), 4)
+            for i in range(len(ops)) if ops[i][2] != "other"}
+    return {"steps": n, "seconds": round(total / 1e3, 3), "ms_per_step": round(total / n, 3),
+            "clocks": sampler.summary(), "last_steps_ms": last}
 
 
 def _time_op(f, reps: int, stream, warmup: int = 3) -> float:

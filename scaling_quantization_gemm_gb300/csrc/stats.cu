@@ -126,32 +126,36 @@ __global__ void __launch_bounds__(kStatsThreads)
     cast_stats_kernel(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, const float* scales, int n,
                       unsigned long long* saturated, unsigned long long* underflow) {
     __shared__ uint32_t sT[NS], sU[NS];
-    __shared__ uint32_t red[kStatsThreads / 32][2 * NS];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // this CTA's counts: saturated per scale, |x| <= U_j per scale, zeros
+    __shared__ unsigned long long cnt[2 * NS + 1];
+    const int tid = threadIdx.x, lane = tid & 31;
     if (tid < NS) {
         uint32_t t = kInfMag + 1, u = 0;  // padding slots match nothing
         if (tid < n) thresholds<FMT>(scales[tid], t, u);
         sT[tid] = t;
         sU[tid] = u;
     }
+    if (tid < 2 * NS + 1) cnt[tid] = 0;
     __syncthreads();
-    uint32_t T2[NS], U2[NS], cs[NS], cu[NS], ps[NS], pu[NS], pz = 0, cz = 0;
+    uint32_t T2[NS], U2[NS], ps[NS], pu[NS], pz = 0;
 #pragma unroll
     for (int j = 0; j < NS; ++j) {
         T2[j] = sT[j] * 0x10001u;
         U2[j] = sU[j] * 0x10001u;
-        cs[j] = cu[j] = ps[j] = pu[j] = 0;
+        ps[j] = pu[j] = 0;
     }
-    // a packed lane counts at most 16 per step (four 16-byte chunks): fold the lanes into 32-bit counts
-    // every 2048 steps
-    auto fold = [&]() {
+    // a packed lane counts at most 16 per step (four 16-byte chunks): every 2048 steps a thread adds its
+    // lanes into the CTA's counts (tensors of more than 2048 steps per thread only), and once at the end
+    auto fold_thread = [&]() {
 #pragma unroll
         for (int j = 0; j < NS; ++j) {
-            cs[j] += down_count(ps[j]);
-            cu[j] += down_count(pu[j]);
+            const uint32_t a = down_count(ps[j]), b = down_count(pu[j]);
+            if (a) atomicAdd(&cnt[j], (unsigned long long)a);
+            if (b) atomicAdd(&cnt[NS + j], (unsigned long long)b);
             ps[j] = pu[j] = 0;
         }
-        cz += down_count(pz);
+        const uint32_t z = down_count(pz);
+        if (z) atomicAdd(&cnt[2 * NS], (unsigned long long)z);
         pz = 0;
     };
     const int64_t cpr = cols >> 3;
@@ -176,30 +180,25 @@ __global__ void __launch_bounds__(kStatsThreads)
         count8(v2);
         count8(v3);
         if (++steps == 2048) {
-            fold();
+            fold_thread();
             steps = 0;
         }
     }
     for (; i < total; i += stride) count8(ld_stream_v4(addr(i)));  // fewer than four steps: no fold needed
-    fold();
-#pragma unroll
-    for (int j = 0; j < NS; ++j) cu[j] -= cz;  // |x| <= U_j counted the zeros too
+    // every lane is here: one sum per warp and count, one shared atomic
 #pragma unroll
     for (int j = 0; j < NS; ++j) {
-        cs[j] = __reduce_add_sync(0xffffffffu, cs[j]);
-        cu[j] = __reduce_add_sync(0xffffffffu, cu[j]);
+        const uint32_t a = __reduce_add_sync(0xffffffffu, down_count(ps[j]));
+        const uint32_t b = __reduce_add_sync(0xffffffffu, down_count(pu[j]));
+        if (lane == 0 && a) atomicAdd(&cnt[j], (unsigned long long)a);
+        if (lane == 0 && b) atomicAdd(&cnt[NS + j], (unsigned long long)b);
     }
-    if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < NS; ++j) {
-            red[warp][j] = cs[j];
-            red[warp][NS + j] = cu[j];
-        }
-    }
+    const uint32_t z = __reduce_add_sync(0xffffffffu, down_count(pz));
+    if (lane == 0 && z) atomicAdd(&cnt[2 * NS], (unsigned long long)z);
     __syncthreads();
     if (tid < 2 * NS && (tid % NS) < n) {
-        unsigned long long sum = 0;
-        for (int w = 0; w < kStatsThreads / 32; ++w) sum += red[w][tid];
+        // |x| <= U_j counted the zeros too
+        const unsigned long long sum = tid < NS ? cnt[tid] : cnt[tid] - cnt[2 * NS];
         if (sum) atomicAdd(tid < NS ? &saturated[tid] : &underflow[tid - NS], sum);
     }
 }
@@ -225,10 +224,17 @@ fp8_status launch_stats(const void* x, int64_t rows, int64_t cols, int64_t ld, c
 template <int FMT>
 fp8_status launch_stats_fmt(const void* x, int64_t rows, int64_t cols, int64_t ld, const float* scales, int n,
                             uint64_t* saturated, uint64_t* underflow, cudaStream_t st) {
-    if (n <= 1) return launch_stats<FMT, 1>(x, rows, cols, ld, scales, n, saturated, underflow, st);
-    if (n <= 2) return launch_stats<FMT, 2>(x, rows, cols, ld, scales, n, saturated, underflow, st);
-    if (n <= 4) return launch_stats<FMT, 4>(x, rows, cols, ld, scales, n, saturated, underflow, st);
-    return launch_stats<FMT, kMaxScales>(x, rows, cols, ld, scales, n, saturated, underflow, st);
+    // one instantiation per count: a padding slot would cost its compares and adds on every word
+    switch (n) {
+        case 1: return launch_stats<FMT, 1>(x, rows, cols, ld, scales, n, saturated, underflow, st);
+        case 2: return launch_stats<FMT, 2>(x, rows, cols, ld, scales, n, saturated, underflow, st);
+        case 3: return launch_stats<FMT, 3>(x, rows, cols, ld, scales, n, saturated, underflow, st);
+        case 4: return launch_stats<FMT, 4>(x, rows, cols, ld, scales, n, saturated, underflow, st);
+        case 5: return launch_stats<FMT, 5>(x, rows, cols, ld, scales, n, saturated, underflow, st);
+        case 6: return launch_stats<FMT, 6>(x, rows, cols, ld, scales, n, saturated, underflow, st);
+        case 7: return launch_stats<FMT, 7>(x, rows, cols, ld, scales, n, saturated, underflow, st);
+        default: return launch_stats<FMT, kMaxScales>(x, rows, cols, ld, scales, n, saturated, underflow, st);
+    }
 }
 
 }  // namespace

@@ -47,6 +47,19 @@ def test_stats_every_bf16(q, fmt):
         assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), scales
 
 
+@pytest.mark.parametrize("n", range(1, 9))
+def test_stats_every_scale_count(q, n):
+    """Each count of scales (1 to 8) has its own kernel instantiation: all 65536 bf16 patterns, the
+    first n of a list that mixes powers of two with other scales, both formats."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(256, 256)
+    x = dev_bf16(bits)
+    scales = [2.0 ** -3, 0.7, 2.0 ** 5, 1.0, 2.0 ** -20, 3.0, 2.0 ** 12, 1e-3][:n]
+    for fmt in (0, 1):
+        got = gpu_stats(q, x, fmt, scales)
+        ref = oracle.cast_stats(bits, fmt, scales)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), (fmt, scales)
+
+
 @pytest.mark.parametrize("shape,ld", [((48, 136), 136), ((130, 264), 280), ((1000, 1024), 1024)])
 def test_stats_shapes_and_accumulation(q, shape, ld):
     r, c = shape

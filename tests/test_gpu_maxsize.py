@@ -86,3 +86,27 @@ def test_gemm_output_past_2g_elements(mx):
     assert int(host(status)[0]) == 0
     assert_gemm_close(y, y_ref, mag, True)
     del D
+
+
+def test_cast_stats_past_the_counter_fold():
+    """2^34 elements (34 GB of bf16): every thread of the statistics kernel runs more than the 2048
+    steps after which it folds its packed 16-bit lane counters into the CTA's counts.  The tensor is a
+    4-row tile (a saturating row, a row that flushes at the small scales, zeros, the negated second
+    row) repeated down the rows, so the exact counts are the oracle's on the tile times the repeats."""
+    q = require_gpu()
+    C, reps = 32768, 1 << 17
+    a, b = (int(v) for v in wl.bf16_bits(np.array([60000.0, 2.0 ** -18], np.float32)))
+    tile = np.zeros((4, C), np.uint16)
+    tile[0], tile[1], tile[3] = a, b, b | 0x8000
+    tile[0, ::7] = b  # rows that mix both kinds of element
+    x = dev_bf16(tile).repeat(reps, 1)
+    assert x.numel() == 1 << 34
+    for scales in ([2.0 ** e for e in range(-3, 4)], [2.0 ** e for e in (-1, 0, 1, 2)], [1.0, 4.0]):
+        sc = torch.tensor(np.asarray(scales, np.float32), device="cuda")
+        sat = torch.zeros(len(scales), dtype=torch.int64, device="cuda")
+        und = torch.zeros(len(scales), dtype=torch.int64, device="cuda")
+        q.fp8_cast_stats(x, q.E5M2, sc, sat, und)
+        ref_s, ref_u = oracle.cast_stats(tile, 1, scales)
+        assert np.array_equal(host(sat).astype(np.uint64), ref_s * np.uint64(reps)), scales
+        assert np.array_equal(host(und).astype(np.uint64), ref_u * np.uint64(reps)), scales
+    del x
