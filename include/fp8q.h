@@ -353,7 +353,8 @@ FP8Q_API fp8_status fp8_quantize_f32(const float *x, int64_t n, fp8_format fmt, 
  *   amax       device fp32 or NULL (written, not accumulated: max|x|).
  *   bias, scale, scale_inv: device, or NULL, as for fp8_compute_scale.
  *   workspace  device, FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES bytes, 16-byte
- *              aligned, owned by the caller.  Zero it once before its first
+ *              aligned, owned by the caller (the grid barrier uses its first
+ *              16 bytes; the rest is reserved).  Zero it once before its first
  *              use; every call leaves it ready for the next one.  Calls that
  *              share a workspace must not run at the same time (same stream,
  *              or ordered by events).  After a call that reported
@@ -379,10 +380,10 @@ FP8Q_API fp8_status fp8_quantize_current(const void *x, int64_t rows, int64_t co
  * nothing.
  *
  * Arguments and results are those of fp8_quantize_current, without
- * `workspace`.  The scratch is a static 4 KB array in the library's device
- * code, present on every GPU that loads the library until the process exits.
- * It holds one slot per CTA, so the launch uses at most 1020 CTAs (fewer than
- * would fit on a GPU with more resident CTAs; GB300 uses 456).
+ * `workspace`.  The scratch is a static 256-byte array in the library's device
+ * code (the grid barrier's 16-byte header: arrival count, generation, scale and
+ * the running max), present on every GPU that loads the library until the
+ * process exits.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make that
  *     first call before any stream capture.

@@ -146,6 +146,13 @@ __device__ __forceinline__ float bf16bits_to_float(uint32_t b) { return __uint_a
 
 // --------------------------------------------------------------- memory
 
+// 16-byte global store with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void st_global_v4_hint(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                  uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(a), "r"(b), "r"(c),
+                 "r"(d), "l"(policy)
+                 : "memory");
+}
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -253,6 +260,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int x, int y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"((uint64_t)map),
                  "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+// Same, with an L2 cache policy (from createpolicy) attached to the store.
+__device__ __forceinline__ void tma_store_2d_hint(const void* map, uint32_t src, int x, int y, uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
+                     (uint64_t)map),
+                 "r"(x), "r"(y), "r"(src), "l"(policy)
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

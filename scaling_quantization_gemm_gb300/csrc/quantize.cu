@@ -213,8 +213,12 @@ __device__ __forceinline__ void stage_col32(uint32_t base, int c, int seg, const
 // conflicts.
 // The tile loop (shared by the cast kernel and the fused current-scaling kernel).  For
 // per-tensor scaling `s_given` is the scale; block granularities compute their own.  With
-// `from_end` the CTAs walk the tiles from the last one back (the fused kernel's amax pass reads x
-// front to back, so the tiles it read last are the likeliest to be still in L2).
+// `from_end` (the fused kernel, whose amax pass has just read x front to back) the CTAs walk the
+// tiles from the last one back, so that the tiles read last, the likeliest to be still in L2, come
+// first, and the codes are stored with an L2 evict-first policy, so that they do not push the rest
+// of x out of L2 before it is read again (measured: 92.2 -> 88.1 us at 16384x5120 row+col).  The
+// plain casts store without the hint: their codes are the next GEMM's operands (measured: the hint
+// made the benchmark step's casts 1 % slower).
 template <int GRAN, int FMT>
 __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const QuantArgs& a, float s_given, int cta,
                                                int ctas, bool from_end = false) {
@@ -252,6 +256,7 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
     // outputs (measured: row+col per-tensor cast 6 % faster); the block granularities measured
     // slower with the hint and load without it.
     const uint64_t policy = GRAN == FP8_SCALE_TENSOR && tid == 0 ? l2_policy_evict_first() : 0;
+    const uint64_t out_policy = from_end ? l2_policy_evict_first() : 0;
     // Tile coordinates (tile row, tile column) advance by the grid size each step, with a carry: one
     // division per CTA instead of a 64-bit division per tile in every thread.
     const int tiles_c = (int)a.tiles_c;
@@ -409,7 +414,10 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
                     }
                     uint8_t* dst = dst_row;
                     if (cc + 16 <= a.cols && rows16) {
-                        *reinterpret_cast<uint4*>(dst) = make_uint4(q0.x, q0.y, q1.x, q1.y);
+                        if (from_end)
+                            st_global_v4_hint(dst, q0.x, q0.y, q1.x, q1.y, out_policy);
+                        else
+                            *reinterpret_cast<uint4*>(dst) = make_uint4(q0.x, q0.y, q1.x, q1.y);
                     } else {
                         if (cc < a.cols) *reinterpret_cast<uint2*>(dst) = q0;
                         if (cc + 8 < a.cols) *reinterpret_cast<uint2*>(dst + 8) = q1;
@@ -494,7 +502,10 @@ __device__ __forceinline__ void quantize_tiles(const QuantMaps* maps, const Quan
             fence_proxy_async_smem();
             __syncthreads();
             if (tid == 0) {
-                tma_store_2d(&maps->qc, Tb, (int)r0, (int)c0);
+                if (from_end)
+                    tma_store_2d_hint(&maps->qc, Tb, (int)r0, (int)c0, out_policy);
+                else
+                    tma_store_2d(&maps->qc, Tb, (int)r0, (int)c0);
                 bulk_commit();
             }
         }
@@ -587,20 +598,21 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_batch_kernel(const __gri
 // ------------------------------------------------- fused current scaling
 
 // Per-tensor current scaling in one cooperative launch: amax of x, the
-// compute_bias rule, and the cast with 2^e.  Phase 1 reduces max|x| per CTA
-// into the workspace; the last CTA to reach the grid barrier reduces those,
-// derives e, writes the caller's amax / bias / scale / scale_inv, publishes 2^e
-// and releases the others (a generation counter, so the workspace is left
-// ready for the next call); phase 2 is the tile loop of the cast kernel.
+// compute_bias rule, and the cast with 2^e.  Phase 1 reduces max|x| per CTA and
+// folds it into one workspace word with an atomic max; the last CTA to reach
+// the grid barrier reads that word, derives e, writes the caller's amax / bias /
+// scale / scale_inv, publishes 2^e and releases the others (a generation
+// counter; it zeroes the max and the count, so the workspace is left ready for
+// the next call); phase 2 is the tile loop of the cast kernel.  One word instead
+// of a slot per CTA that the last CTA reads one by one: 10-12 us less per call.
 struct CurrentWorkspace {
-    unsigned count;   // CTAs arrived at the barrier of the current call
-    unsigned gen;     // barrier generation
-    float scale;      // 2^e of the current call
-    unsigned pad;
-    unsigned partial[1];  // per-CTA max |x| (bf16 magnitude bits), one per CTA
+    unsigned count;      // CTAs arrived at the barrier of the current call
+    unsigned gen;        // barrier generation
+    float scale;         // 2^e of the current call
+    unsigned amax_bits;  // max |x| of the current call (bf16 magnitude bits, NaN above inf); 0 at rest
 };
 constexpr int kCurrentWsHeader = 16;
-constexpr int kCurrentMaxCtas = (FP8_QUANTIZE_CURRENT_WORKSPACE_BYTES - kCurrentWsHeader) / 4;
+static_assert(sizeof(CurrentWorkspace) == kCurrentWsHeader, "barrier header layout");
 
 struct CurrentOut {
     float* amax;
@@ -651,13 +663,13 @@ __global__ void __launch_bounds__(kThreads, 3)
         for (int w = 1; w < kThreads / 32; ++w) mx = max(mx, red[w]);
         volatile CurrentWorkspace* vws = ws;
         const unsigned gen0 = vws->gen;
-        vws->partial[blockIdx.x] = mx;
+        atomicMax(&ws->amax_bits, mx);  // before this CTA counts itself in
         __threadfence();
         s_abort = 0;
         if (atomicAdd(&ws->count, 1u) == gridDim.x - 1) {
             __threadfence();
-            uint32_t all = 0;
-            for (unsigned c = 0; c < gridDim.x; ++c) all = max(all, vws->partial[c]);
+            const uint32_t all = vws->amax_bits;  // every CTA's max arrived before its count
+            vws->amax_bits = 0;
             const float amax = bf16bits_to_float(all);
             bool nf = false;
             const int e = bias_from_amax(amax, FMT, out.margin, &nf);
@@ -1014,11 +1026,9 @@ fp8_status launch_current(const QuantMaps& tm, const QuantArgs& a, const void* x
     int occ = 0;
     fp8_status s = resident_ctas(reinterpret_cast<const void*>(k), kThreads, smem, &occ);
     if (s != FP8_OK) return s;
-    // every CTA must be resident at once (grid barrier): at most SMs x occupancy, and one
-    // workspace slot per CTA
+    // every CTA must be resident at once (grid barrier): at most SMs x occupancy
     int64_t grid = (int64_t)device_sm_count() * occ;
     if (grid > a.ntiles) grid = a.ntiles;
-    if (grid > kCurrentMaxCtas) grid = kCurrentMaxCtas;
     if (grid < 1) grid = 1;
     QuantMaps tm_arg = tm;
     QuantArgs a_arg = a;
@@ -1144,23 +1154,21 @@ fp8_status launch_quantize_current(const void* x, int64_t rows, int64_t cols, in
 // ------------------------------------------- fused current scaling, no allocation
 //
 // fp8_quantize_current_noalloc runs the same kernel as fp8_quantize_current, with
-// its barrier counters and per-CTA partials in the library's own static device
-// array instead of a caller workspace.  It is for callers that cannot allocate
+// its barrier header in the library's own static device array instead of a
+// caller workspace.  It is for callers that cannot allocate
 // device memory at the point of the call: a plugin or callback that a host
 // framework hands only its input and output buffers, code whose device memory is
 // planned once at start-up against a fixed budget, and latency-bound loops that
 // cannot take the device-wide synchronisation cudaMalloc / cudaFree may cause.
 //
-// The array is kNoAllocScratchBytes (4 KB) on every GPU that loads the library,
-// held until the process exits: a 16-byte header (arrival count, generation,
-// scale) and one 4-byte partial per CTA, so at most (4096 - 16) / 4 = 1020 CTAs;
-// the grid is capped there (GB300 runs 456).  Every call shares the array and
-// finds the previous call's contents there; the call clears the header on its
-// stream before the kernel, and each CTA writes its partial before any CTA reads
-// it.  Calls whose kernels overlap on the GPU (other streams, other host threads)
-// race on the array.
-constexpr int kNoAllocScratchBytes = 4096;
-constexpr int kNoAllocMaxCtas = (kNoAllocScratchBytes - kCurrentWsHeader) / 4;
+// The array is kNoAllocScratchBytes (256 bytes) on every GPU that loads the
+// library, held until the process exits; the kernel uses its 16-byte header
+// (arrival count, generation, scale, the atomic max).  Every call shares the
+// array and finds the previous call's contents there; the call clears the header
+// on its stream before the kernel.  Calls whose kernels overlap on the GPU (other
+// streams, other host threads) race on the array.
+constexpr int kNoAllocScratchBytes = 256;
+static_assert(kNoAllocScratchBytes >= kCurrentWsHeader, "scratch holds the barrier header");
 static __device__ __align__(256) unsigned char g_current_scratch[kNoAllocScratchBytes];
 
 namespace {
@@ -1201,13 +1209,7 @@ fp8_status launch_current_noalloc(const QuantMaps& tm, const QuantArgs& a, const
     if (s != FP8_OK) return s;
     int64_t grid = (int64_t)device_sm_count() * occ;  // all CTAs resident at once (grid barrier)
     if (grid > a.ntiles) grid = a.ntiles;
-    // one scratch slot per CTA: fewer CTAs than fit only lengthen each CTA's grid-stride loops
-    if (grid > kNoAllocMaxCtas) grid = kNoAllocMaxCtas;
     if (grid < 1) grid = 1;
-    const int64_t need = kCurrentWsHeader + 4 * grid;
-    FP8_REQUIRE(need <= kNoAllocScratchBytes, FP8_ERR_UNSUPPORTED,
-                "this launch needs %lld bytes of scratch (%lld CTAs); the static array holds %d bytes (%d CTAs)",
-                (long long)need, (long long)grid, kNoAllocScratchBytes, (kNoAllocScratchBytes - kCurrentWsHeader) / 4);
     cudaError_t e = cudaMemsetAsync(scratch, 0, kCurrentWsHeader, st);
     FP8_REQUIRE(e == cudaSuccess, FP8_ERR_CUDA, "cudaMemsetAsync(scratch header): %s", cudaGetErrorString(e));
     QuantMaps tm_arg = tm;
