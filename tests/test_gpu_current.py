@@ -85,9 +85,10 @@ def test_many_ctas_and_repeated_calls_share_a_workspace(q):
         xb = wl.delayed_activation(t) if t % 2 == 0 else wl.random_bf16(500 + t, 4096, 4096, "laplace", 10.0 ** (t - 5))
         o.run(q, dev_bf16(xb), t % 2, t % 2, ws)
         check(o, xb, t % 2, t % 2)
-    hdr = host(ws[:8].view(torch.int32))
+    hdr = host(ws[:16].view(torch.int32))
     assert hdr[0] == 0  # arrival count back to zero
     assert hdr[1] == 10  # one barrier generation per call
+    assert hdr[3] == 0  # the running max (the CTAs' atomic max) zeroed for the next call
 
 
 def test_matches_the_three_call_path(q):
